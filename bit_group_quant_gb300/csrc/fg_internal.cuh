@@ -1,0 +1,261 @@
+// fg_internal.cuh -- shared device helpers (inline PTX for mbarrier, TMA and
+// tcgen05) and host-side declarations used across libfg's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fg.h"
+
+namespace fg {
+
+constexpr int kGroup = 64;                 // quantisation group (elements)
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s per bounded wait
+constexpr int kNumSMsHint = 152;
+
+// Device status codes written by kernels (first error wins).
+constexpr int kDevTimeout = 1;
+
+// ---------------------------------------------------------------- host side
+
+fg_status set_error(fg_status s, const char* fmt, ...);
+fg_status cuda_error(cudaError_t e, const char* what);
+int* device_status_ptr();                  // per current device, never NULL on success
+uint64_t wait_limit_ns();
+int take_drop_arrive();                    // test knob: consumed by the next GEMM launch
+int num_sms();
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Launchers implemented in the kernel translation units.  All validate
+// nothing: the exported entry points validate first.
+fg_status launch_quantize_g4(const __half* x, int64_t ngroups, uint8_t* codes, float* meta,
+                             cudaStream_t st);
+fg_status launch_dequant_g4(const uint8_t* codes, const float* meta, int64_t ngroups,
+                            __half* x, cudaStream_t st);
+fg_status launch_kv_store(const __half* qkv, int64_t ld, int32_t B, int32_t T, int32_t H,
+                          int32_t d, const fg_kv4* c, int32_t slot0, cudaStream_t st);
+fg_status launch_layernorm(const __half* x, int64_t rows, int64_t cols, int64_t x_ld,
+                           const __half* g, const __half* b, float eps, __half* y,
+                           cudaStream_t st);
+fg_status launch_embed(const int32_t* ids, int64_t ntok, int32_t T, int32_t pos0,
+                       const __half* e_tok, const __half* e_pos, int32_t h1, __half* y,
+                       cudaStream_t st);
+fg_status launch_decode_attn(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
+                             int32_t fuse_append, __half* out, cudaStream_t st);
+fg_status launch_prefill_attn(const __half* qkv, int32_t B, int32_t s, int32_t H, int32_t d,
+                              __half* out, cudaStream_t st);
+
+struct GemmPlan {
+    int nt;          // activation rows per tile (MMA N), multiple of 16, <= 256
+    int tok_tiles;
+    int feat_tiles;  // ceil(N / 128)
+    int splits;      // K splits (grid.z); > 1 only when tok_tiles == 1
+    size_t ws_bytes; // fp32 partial sums when splits > 1
+};
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K);
+fg_status launch_gemm_g4(const __half* X, int64_t M, const fg_q4* W, const __half* bias,
+                         const __half* residual, int act, __half* Y, void* ws, size_t ws_bytes,
+                         cudaStream_t st);
+fg_status launch_gemm_f16_f32out(const __half* X, int64_t M, const __half* W, int64_t N,
+                                 int64_t K, float* Y, cudaStream_t st);
+
+}  // namespace fg
+
+// ---------------------------------------------------------------- device side
+namespace fgd {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void report(int* status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// ---- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with the given parity to complete.  Returns
+// false if the time limit passes or, when `abort` is not null, another role
+// of the CTA raised *abort.  Drains of work already in flight pass a null
+// `abort` so that they end only on completion or on the time limit.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 31u) == 0) {
+            if (abort != nullptr && *abort) return false;
+            if (globaltimer() - t0 > limit_ns) return false;
+        }
+    }
+}
+
+// ---- TMA (bulk tensor copies, no multicast)
+__device__ __forceinline__ void prefetch_tmap(const void* tm) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tm, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(tm), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- tcgen05 (5th-generation tensor cores, accumulators in TMEM)
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on an mbarrier when all previously issued tcgen05 ops of this
+// thread have completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+// 32 lanes x 32 bit, 16 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%"
+        "14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand tile stored with the
+// 128-byte swizzle: rows of 128 bytes (64 fp16), 8-row atoms of 1024 bytes.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);      // start address
+    d |= static_cast<uint64_t>(16u >> 4) << 16;                 // leading byte offset (unused)
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;               // stride byte offset: 8 rows
+    d |= static_cast<uint64_t>(1) << 46;                        // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                        // 128-byte swizzle
+    return d;
+}
+// Instruction descriptor: fp16 A and B (K-major), fp32 D, shape M x N.
+__device__ __forceinline__ uint32_t idesc_f16_f32(int M, int N) {
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ---- IEEE total order helpers (finite values): -0 below +0.
+__device__ __forceinline__ bool total_less(float a, float b) {
+    return a < b || (a == b && (__float_as_uint(a) >> 31) > (__float_as_uint(b) >> 31));
+}
+__device__ __forceinline__ float tmin(float a, float b) { return total_less(b, a) ? b : a; }
+__device__ __forceinline__ float tmax(float a, float b) { return total_less(a, b) ? b : a; }
+
+// Quantise one group of 64 values held by 8 consecutive lanes (8 values per
+// lane, lane8 = lane & 7 holds elements 8*lane8 .. 8*lane8+7).  Returns the
+// 8 codes packed into one word (element 8*lane8 in the lowest nibble) and
+// writes (min, scale) of the group.  Matches the definition bit for bit:
+// fp32 min/max in the IEEE total order, scale = (M - m) / 15 (IEEE divide),
+// code = clamp(rint((x - m) / scale), 0, 15), all zero when scale == 0.
+__device__ __forceinline__ uint32_t quantize8(const float (&v)[8], float& mn_out,
+                                              float& scale_out) {
+    float mn = v[0], mx = v[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) {
+        mn = tmin(mn, v[i]);
+        mx = tmax(mx, v[i]);
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        mn = tmin(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = tmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    const float scale = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
+    uint32_t packed = 0;
+    if (scale != 0.0f) {
+        const float inv = __frcp_rn(scale);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float num = __fsub_rn(v[i], mn);
+            // Fast quotient (within 2 ulp of the IEEE quotient); where it lies
+            // that close to a rounding tie, take the IEEE division itself.
+            float t = __fmul_rn(num, inv);
+            const float frac = t - floorf(t);
+            if (fabsf(frac - 0.5f) < 1.0f / 65536.0f) t = __fdiv_rn(num, scale);
+            float r = rintf(t);
+            r = fminf(fmaxf(r, 0.0f), 15.0f);
+            packed |= static_cast<uint32_t>(r) << (4 * i);
+        }
+    }
+    mn_out = mn;
+    scale_out = scale;
+    return packed;
+}
+
+}  // namespace fgd

@@ -1,0 +1,149 @@
+// small.cu -- LayerNorm and token + position embedding (the OPT layer's
+// pre-LN normalisations and the model input).  Both are bandwidth-trivial
+// next to the projections; one CTA per row keeps the row in registers.
+#include "fg_internal.cuh"
+
+namespace {
+
+constexpr int kLnThreads = 256;
+constexpr int kLnMaxVec = 8;   // up to 8 x 8 x 256 = 16384 columns held in registers
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    float t = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kLnThreads / 32; ++i) t += red[i];
+    return t;
+}
+
+// y = (x - mean) / sqrt(var + eps) * gamma + beta; mean, biased variance fp32.
+__global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const __half* __restrict__ x,
+                                                               int64_t cols, int64_t x_ld,
+                                                               const __half* __restrict__ g,
+                                                               const __half* __restrict__ b,
+                                                               float eps, __half* __restrict__ y) {
+    __shared__ float red[kLnThreads / 32];
+    const int64_t row = blockIdx.x;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * x_ld);
+    const int nvec = static_cast<int>(cols / 8);
+    float v[kLnMaxVec][8];
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kLnMaxVec; ++i) {
+        const int c = threadIdx.x + i * kLnThreads;
+        if (c < nvec) {
+            const uint4 raw = xr[c];
+            const __half2* h = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = __half22float2(h[j]);
+                v[i][2 * j] = f.x;
+                v[i][2 * j + 1] = f.y;
+                s += f.x + f.y;
+            }
+        }
+    }
+    const float mean = __fdiv_rn(block_sum(s, red), static_cast<float>(cols));
+    float q = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kLnMaxVec; ++i) {
+        const int c = threadIdx.x + i * kLnThreads;
+        if (c < nvec) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float dv = __fsub_rn(v[i][j], mean);
+                q = __fadd_rn(q, __fmul_rn(dv, dv));
+            }
+        }
+    }
+    const float var = __fdiv_rn(block_sum(q, red), static_cast<float>(cols));
+    const float denom = __fsqrt_rn(__fadd_rn(var, eps));
+    uint4* yr = reinterpret_cast<uint4*>(y + row * cols);
+    const uint4* gr = reinterpret_cast<const uint4*>(g);
+    const uint4* br = reinterpret_cast<const uint4*>(b);
+#pragma unroll
+    for (int i = 0; i < kLnMaxVec; ++i) {
+        const int c = threadIdx.x + i * kLnThreads;
+        if (c < nvec) {
+            const uint4 graw = gr[c], braw = br[c];
+            const __half2* gh = reinterpret_cast<const __half2*>(&graw);
+            const __half2* bh = reinterpret_cast<const __half2*>(&braw);
+            uint4 out;
+            __half2* oh = reinterpret_cast<__half2*>(&out);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 gf = __half22float2(gh[j]);
+                const float2 bf = __half22float2(bh[j]);
+                const float a0 = __fadd_rn(
+                    __fmul_rn(__fdiv_rn(__fsub_rn(v[i][2 * j], mean), denom), gf.x), bf.x);
+                const float a1 = __fadd_rn(
+                    __fmul_rn(__fdiv_rn(__fsub_rn(v[i][2 * j + 1], mean), denom), gf.y), bf.y);
+                oh[j] = __halves2half2(__float2half_rn(a0), __float2half_rn(a1));
+            }
+            yr[c] = out;
+        }
+    }
+}
+
+// y[r] = e_tok[ids[r]] + e_pos[pos0 + r % T]  (fp32 add, one rounding).
+__global__ void __launch_bounds__(256) embed_kernel(const int32_t* __restrict__ ids, int64_t ntok,
+                                                    int32_t T, int32_t pos0,
+                                                    const __half* __restrict__ e_tok,
+                                                    const __half* __restrict__ e_pos, int32_t h1,
+                                                    __half* __restrict__ y) {
+    const int64_t nvec = static_cast<int64_t>(h1) / 8;
+    const int64_t total = ntok * nvec;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / nvec, c = i % nvec;
+        const int64_t id = ids[r];
+        const int64_t p = pos0 + r % T;
+        const uint4 a = reinterpret_cast<const uint4*>(e_tok + id * h1)[c];
+        const uint4 bb = reinterpret_cast<const uint4*>(e_pos + p * h1)[c];
+        const __half2* ah = reinterpret_cast<const __half2*>(&a);
+        const __half2* bh = reinterpret_cast<const __half2*>(&bb);
+        uint4 out;
+        __half2* oh = reinterpret_cast<__half2*>(&out);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 af = __half22float2(ah[j]);
+            const float2 bf = __half22float2(bh[j]);
+            oh[j] = __halves2half2(__float2half_rn(__fadd_rn(af.x, bf.x)),
+                                   __float2half_rn(__fadd_rn(af.y, bf.y)));
+        }
+        reinterpret_cast<uint4*>(y + r * h1)[c] = out;
+    }
+}
+
+}  // namespace
+
+namespace fg {
+
+fg_status launch_layernorm(const __half* x, int64_t rows, int64_t cols, int64_t x_ld,
+                           const __half* g, const __half* b, float eps, __half* y,
+                           cudaStream_t st) {
+    if (rows == 0) return FG_OK;
+    if (cols > static_cast<int64_t>(kLnMaxVec) * 8 * kLnThreads)
+        return set_error(FG_ERR_UNSUPPORTED, "layernorm: cols %lld > %d", (long long)cols,
+                         kLnMaxVec * 8 * kLnThreads);
+    layernorm_kernel<<<static_cast<unsigned>(rows), kLnThreads, 0, st>>>(x, cols, x_ld, g, b, eps, y);
+    return cuda_error(cudaGetLastError(), "layernorm launch");
+}
+
+fg_status launch_embed(const int32_t* ids, int64_t ntok, int32_t T, int32_t pos0,
+                       const __half* e_tok, const __half* e_pos, int32_t h1, __half* y,
+                       cudaStream_t st) {
+    if (ntok == 0) return FG_OK;
+    int64_t blocks = cdiv(ntok * (h1 / 8), 256);
+    if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
+    embed_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(ids, ntok, T, pos0, e_tok, e_pos,
+                                                                h1, y);
+    return cuda_error(cudaGetLastError(), "embed launch");
+}
+
+}  // namespace fg

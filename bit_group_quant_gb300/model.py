@@ -1,0 +1,183 @@
+"""OPT decoder driver over libfg: weights stored 4-bit and resident in HBM,
+a 4-bit KV cache, and generation under the block schedule.
+
+Torch supplies device memory, streams and the synthetic inputs; every step
+of prefill and decode is a libfg call (embedding, layer steps, final
+LayerNorm, LM head).  Schedule ("FlexGen 完全拆解", computation-graph
+section): for each token step and each layer, the k GPU batches of the block
+pass through that layer's weights before the next layer; with order "block"
+the k batches are one launch per projection (weights read once per block),
+with order "zigzag" they are k launches whose order reverses at every token
+step.  The first generated token comes from the prefill, so n tokens take
+n-1 decode steps.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import fg
+import synth
+
+
+@dataclass
+class Layer:
+    qkv: fg.Q4
+    out: fg.Q4
+    fc1: fg.Q4
+    fc2: fg.Q4
+    b_qkv: torch.Tensor
+    b_out: torch.Tensor
+    b_fc1: torch.Tensor
+    b_fc2: torch.Tensor
+    ln1_g: torch.Tensor
+    ln1_b: torch.Tensor
+    ln2_g: torch.Tensor
+    ln2_b: torch.Tensor
+    h1: int
+    H: int
+    h2: int
+    eps: float = 1e-5
+
+    def c(self) -> fg.c_layer:
+        p = lambda t: t.data_ptr()
+        return fg.c_layer(self.qkv.c(), self.out.c(), self.fc1.c(), self.fc2.c(),
+                          p(self.b_qkv), p(self.b_out), p(self.b_fc1), p(self.b_fc2),
+                          p(self.ln1_g), p(self.ln1_b), p(self.ln2_g), p(self.ln2_b),
+                          self.h1, self.H, self.h2, self.eps)
+
+    @property
+    def nbytes_q4(self):
+        return self.qkv.nbytes + self.out.nbytes + self.fc1.nbytes + self.fc2.nbytes
+
+
+def quantize_layer(w: dict, h1: int, H: int, h2: int, eps: float = 1e-5) -> Layer:
+    """w: fp16 CUDA tensors (torch Linear layout).  The projections are
+    quantised on the GPU by fg_quantize_g4; the fp16 copies can be dropped."""
+    q = lambda name: fg.fg_quantize_g4(w[name].contiguous())
+    c = lambda name: w[name].contiguous()
+    return Layer(q("w_qkv"), q("w_out"), q("w_fc1"), q("w_fc2"), c("b_qkv"), c("b_out"),
+                 c("b_fc1"), c("b_fc2"), c("ln1_g"), c("ln1_b"), c("ln2_g"), c("ln2_b"),
+                 h1, H, h2, eps)
+
+
+def order_for(step: int, order: str) -> int:
+    if order == "block":
+        return fg.FG_ORDER_BLOCK
+    if order == "batches":
+        return fg.FG_ORDER_BATCHES
+    if order == "zigzag":
+        return fg.FG_ORDER_BATCHES if step % 2 == 0 else fg.FG_ORDER_BATCHES_REV
+    raise ValueError(order)
+
+
+class LayerStack:
+    """l decoder layers with their KV caches and one shared workspace for a
+    block of bls = gbs * k sequences."""
+
+    def __init__(self, layers, gbs: int, k: int, cap: int, device="cuda"):
+        self.layers = layers
+        self.c_layers = [L.c() for L in layers]
+        self.gbs, self.k, self.cap = gbs, k, cap
+        L0 = layers[0]
+        self.h1, self.H, self.h2 = L0.h1, L0.H, L0.h2
+        self.d = self.h1 // self.H
+        self.device = device
+        self.caches = [fg.KV4.empty(self.bls, self.H, self.d, cap, device) for _ in layers]
+        self._ws = {}
+
+    @property
+    def bls(self):
+        return self.gbs * self.k
+
+    def policy(self, order_code: int) -> fg.c_policy:
+        return fg.c_policy(self.gbs, self.k, order_code)
+
+    def workspace(self, phase, T, order_code):
+        key = (phase, T, order_code != fg.FG_ORDER_BLOCK)
+        if key not in self._ws:
+            n = fg.fg_layer_workspace_bytes(self.c_layers[0], phase, self.bls, T,
+                                            self.policy(order_code))
+            self._ws[key] = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+        return self._ws[key]
+
+    def run(self, x, phase, T, pos, order_code, out=None, stream=None):
+        """x: [bls*T][h1] fp16 -> hidden states after every layer."""
+        ws = self.workspace(phase, T, order_code)
+        pol = self.policy(order_code)
+        bufs = [out if out is not None else torch.empty_like(x), torch.empty_like(x)]
+        n = len(self.c_layers)
+        cur = x
+        for j, Lc in enumerate(self.c_layers):
+            nxt = bufs[(n - 1 - j) % 2]        # the last layer writes bufs[0]
+            fg.fg_layer_step(Lc, self.caches[j], cur, nxt, phase, T, pos, pol, ws, stream)
+            cur = nxt
+        return cur
+
+
+class Model:
+    """Embeddings + LayerStack + final LayerNorm + LM head tied to the token
+    embedding (fp16, not quantised: the size formula M_W leaves the small
+    embedding out)."""
+
+    def __init__(self, stack: LayerStack, e_tok, e_pos, lnf_g, lnf_b, eps=1e-5):
+        self.stack = stack
+        self.e_tok, self.e_pos = e_tok, e_pos
+        self.lnf_g, self.lnf_b, self.eps = lnf_g, lnf_b, eps
+        self.vocab = e_tok.shape[0]
+
+    def head(self, x, rows, x_ld, logits=None, stream=None):
+        h = fg.fg_layernorm(x, self.lnf_g, self.lnf_b, self.eps, rows=rows, x_ld=x_ld,
+                            stream=stream)
+        return fg.fg_gemm_f16_f32out(h, self.e_tok, Y=logits, stream=stream)
+
+    def prefill(self, prompt_ids, order="block", logits=None, stream=None):
+        """prompt_ids: int32 CUDA [bls][s].  Returns fp32 logits [bls][V] of the
+        last prompt position (the first generated token)."""
+        bls, s = prompt_ids.shape
+        x = fg.fg_embed(prompt_ids.reshape(-1), s, 0, self.e_tok, self.e_pos, stream=stream)
+        y = self.stack.run(x, fg.FG_PHASE_PREFILL, s, 0, order_for(0, order), stream=stream)
+        last = y[s - 1:]          # row b of the view starts at (b*s + s-1) * h1
+        return self.head(last, bls, s * self.stack.h1, logits=logits, stream=stream)
+
+    def decode_step(self, ids, t, s, order="block", logits=None, stream=None):
+        """ids: int32 CUDA [bls], fed at position s+t-1 (decode step t >= 1)."""
+        pos = s + t - 1
+        x = fg.fg_embed(ids, 1, pos, self.e_tok, self.e_pos, stream=stream)
+        y = self.stack.run(x, fg.FG_PHASE_DECODE, 1, pos, order_for(t, order), stream=stream)
+        return self.head(y, ids.shape[0], self.stack.h1, logits=logits, stream=stream)
+
+    def generate(self, prompt_ids, decode_ids_tm, order="block", stream=None):
+        """Teacher-forced generation.  prompt_ids: int32 [bls][s]; decode_ids_tm:
+        int32 [D][bls] (time-major, row t-1 fed at decode step t).  Returns
+        [logits of the prefill] + [logits of decode step t for t = 1..D], each
+        fp32 [bls][V] on the device."""
+        s = prompt_ids.shape[1]
+        out = [self.prefill(prompt_ids, order, stream=stream)]
+        for t in range(1, decode_ids_tm.shape[0] + 1):
+            out.append(self.decode_step(decode_ids_tm[t - 1], t, s, order, stream=stream))
+        return out
+
+
+def random_layers(wl, gen, device="cuda", affine=False, n_layers=None):
+    """Random fp16 weights ~N(0, 0.02) per layer, quantised at once on the GPU
+    so the fp16 copy of the whole model never exists."""
+    layers = []
+    for _ in range(wl.layers if n_layers is None else n_layers):
+        w = synth.layer_weights(wl.h1, wl.h2, gen, device)
+        if affine:
+            w.update(synth.random_affine_params(wl.h1, wl.h2, gen, device))
+        layers.append(quantize_layer(w, wl.h1, wl.H, wl.h2))
+        del w
+    return layers
+
+
+def random_model(wl, seed=0, device="cuda", n_layers=None, cap=None):
+    gen = synth.generator(seed, device)
+    layers = random_layers(wl, gen, device, n_layers=n_layers)
+    stack = LayerStack(layers, wl.gbs, wl.k, cap or wl.cap, device)
+    e_tok, e_pos = synth.embeddings(wl.vocab, wl.cap, wl.h1, gen, device)
+    ones = torch.ones(wl.h1, dtype=torch.float16, device=device)
+    zeros = torch.zeros(wl.h1, dtype=torch.float16, device=device)
+    return Model(stack, e_tok, e_pos, ones, zeros)

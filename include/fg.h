@@ -1,0 +1,252 @@
+/*
+ * fg.h -- C ABI of libfg: the GB300 (sm_103a) hot path of 4-bit group-
+ * quantised, block-scheduled OPT decoding.
+ *
+ * What the library computes is defined on the pages it follows:
+ *   "FlexGen 完全拆解" (pinghaoyang.com.cn), sections
+ *     - "权重压缩与 KV Cache 压缩": group-wise asymmetric min/max 4-bit
+ *       quantisation of weights and KV cache, groups of 64 contiguous
+ *       values, dequantisation to FP16 before compute;
+ *     - "从 Transformer 推理的数据流重新定义卸载": prefill Q, K, V
+ *       projections of all prompt tokens; each decode step appends one K/V
+ *       row and attends one query over s+t cached rows;
+ *     - "FlexGen 的核心：计算图分块与张量生命周期": the zig-zag block schedule,
+ *       one layer's weights kept while the k GPU batches of a block
+ *       (bls = gbs * k sequences) pass through it;
+ *   "bjbfmj.com/news/40234", section 6.3: two 4-bit codes per byte plus a
+ *   per-group scale tensor.
+ *
+ * Conventions shared by every call
+ *  - Pointers are DEVICE pointers unless stated otherwise; struct arguments
+ *    themselves live in host memory and are read before the call returns.
+ *  - The caller owns every buffer.  No call allocates or frees device
+ *    memory; scratch space comes from a caller-provided workspace sized by
+ *    the matching *_workspace_bytes query.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *  - Host-side validation runs before any launch; on failure nothing is
+ *    launched and a status is returned.  fg_last_error() gives a one-line
+ *    detail for the calling thread.  A failed launch returns FG_ERR_CUDA.
+ *  - Device-side waits are bounded.  A wait that expires records
+ *    FG_ERR_TIMEOUT in a per-device status word that fg_check() returns
+ *    and clears; until then, launches that wait on the device skip their
+ *    work (their outputs are unspecified).
+ *  - fp16 tensors are IEEE binary16, passed as fg_f16 (uint16_t bit
+ *    patterns, layout-identical to CUDA's __half).
+ *  - 4-bit layout (part of the ABI): for a [rows][cols] tensor grouped
+ *    along cols in groups of 64, codes are [rows][cols/2] bytes, element 2j
+ *    in the low nibble of byte j and element 2j+1 in the high nibble; meta
+ *    is [rows][cols/64][2] fp32 = (min, scale) per group.
+ *  - Inputs must be finite; NaN or Inf inputs give unspecified outputs.
+ */
+#ifndef FG_H
+#define FG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t fg_f16;                 /* IEEE binary16 bit pattern */
+typedef struct CUstream_st* fg_stream;   /* same type as cudaStream_t */
+
+typedef enum fg_status {
+    FG_OK = 0,
+    FG_ERR_NULL = 1,         /* a required pointer is NULL */
+    FG_ERR_SHAPE = 2,        /* a size or index is outside what the call supports */
+    FG_ERR_ALIGN = 3,        /* a pointer or leading dimension is misaligned */
+    FG_ERR_UNSUPPORTED = 4,  /* valid request this build does not implement */
+    FG_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
+    FG_ERR_TIMEOUT = 6,      /* a bounded device-side wait expired */
+    FG_ERR_WORKSPACE = 7     /* workspace missing or smaller than required */
+} fg_status;
+
+/* 4-bit group-quantised matrix [rows][cols], grouped along cols (for a
+ * weight in torch Linear layout [out][in], cols = in = the contraction
+ * dimension K).  cols % 64 == 0.  codes and meta are 16-byte aligned. */
+typedef struct fg_q4 {
+    uint8_t* codes;   /* [rows][cols/2] */
+    float* meta;      /* [rows][cols/64][2] = (min, scale) */
+    int64_t rows;
+    int64_t cols;
+} fg_q4;
+
+/* One layer's 4-bit KV cache for B sequences, H heads of size d, cap slots.
+ * codes [B][H][cap][d/2], meta [B][H][cap][d/64][2]; grouped along the head
+ * dimension (64 values per group).  d in {64, 128}. */
+typedef struct fg_kv4 {
+    uint8_t* k_codes;
+    uint8_t* v_codes;
+    float* k_meta;
+    float* v_meta;
+    int32_t B, H, d, cap;
+} fg_kv4;
+
+/* Block schedule: bls = gbs * k sequences per block.
+ * order FG_ORDER_BLOCK: each projection is ONE launch over all bls rows, so
+ *   each weight tile is fetched from HBM and dequantised once per block.
+ * order FG_ORDER_BATCHES / FG_ORDER_BATCHES_REV: the k GPU batches run as k
+ *   launches per projection in ascending / descending batch order (the
+ *   zig-zag schedule alternates the two at each token step).
+ * Every order gives bit-identical results. */
+enum { FG_ORDER_BLOCK = 0, FG_ORDER_BATCHES = 1, FG_ORDER_BATCHES_REV = 2 };
+typedef struct fg_policy {
+    int32_t gbs;
+    int32_t k;
+    int32_t order;
+} fg_policy;
+
+/* One OPT decoder layer (pre-LayerNorm, ReLU FFN).  qkv: [3*h1][h1] with
+ * rows q | k | v (head h = rows [h*d, (h+1)*d) of each block); out [h1][h1];
+ * fc1 [h2][h1]; fc2 [h1][h2]; biases and LayerNorm parameters fp16. */
+typedef struct fg_layer {
+    fg_q4 qkv, out, fc1, fc2;
+    const fg_f16 *b_qkv, *b_out, *b_fc1, *b_fc2;
+    const fg_f16 *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+    int32_t h1, H, h2;
+    float ln_eps;
+} fg_layer;
+
+enum { FG_PHASE_PREFILL = 0, FG_PHASE_DECODE = 1 };
+enum { FG_ACT_NONE = 0, FG_ACT_RELU = 1 };
+
+/* ------------------------------------------------------------------ misc */
+
+const char* fg_status_str(fg_status s);
+/* Detail of the calling thread's last failed call ("" if none). */
+const char* fg_last_error(void);
+/* ABI version: (major << 16) | minor. */
+int32_t fg_version(void);
+/* Synchronise `stream`, then read and clear the current device's status
+ * word: FG_ERR_TIMEOUT if a bounded device wait expired since the last
+ * check, FG_ERR_CUDA if the stream reports an error, else FG_OK. */
+fg_status fg_check(fg_stream stream);
+
+/* ------------------------------------------------------------------ quantiser */
+
+/* Group-wise 4-bit quantisation ("FlexGen 完全拆解", section on weight and
+ * KV-cache compression; packing per "bjbfmj.com/news/40234" section 6.3).
+ * For each group of 64 consecutive values of a row: m = min, M = max (fp32,
+ * IEEE total order, -0 below +0); scale = (M - m) / 15 (IEEE fp32 divide);
+ * code = clamp(rint((x - m) / scale), 0, 15), all codes 0 when scale == 0.
+ * x: [rows][cols] fp16, 16-byte aligned; cols % 64 == 0.
+ * out: rows/cols must equal (rows, cols); codes/meta 16-byte aligned.
+ * Bit-exact: identical codes, meta and bytes to the reference definition. */
+fg_status fg_quantize_g4(const fg_f16* x, int64_t rows, int64_t cols,
+                         const fg_q4* out, fg_stream stream);
+
+/* Dequantisation x^ = fp16(fma(code, scale, min)) (fp32 fused multiply-add,
+ * one rounding to fp16).  Test and inspection utility: the hot path fuses
+ * dequantisation into its consumers.  x: [rows][cols] fp16. */
+fg_status fg_dequant_g4(const fg_q4* in, fg_f16* x, fg_stream stream);
+
+/* ------------------------------------------------------------------ GEMMs */
+
+/* Y = act(X W^T + bias) + residual, with W stored 4-bit (dequantised to
+ * fp16 on chip, fp16 x fp16 products accumulated in fp32 on the tensor
+ * cores, epilogue in fp32, one rounding to fp16).  This is every projection
+ * of the decoder ("FlexGen 完全拆解", dataflow section: K = XW_K etc.).
+ * X: [M][K] fp16 (K = W->cols), row stride K, 16-byte aligned.
+ * W: [N][K] 4-bit (N = W->rows).  bias: [N] fp16 or NULL.
+ * residual: [M][N] fp16 or NULL (may alias neither X nor Y).
+ * act: FG_ACT_NONE or FG_ACT_RELU (applied to acc + bias, before residual).
+ * Y: [M][N] fp16.  M >= 0 (M == 0 launches nothing); N % 16 == 0.
+ * workspace: device scratch of at least
+ * fg_dequant_gemm_workspace_bytes(M, N, K) bytes (NULL allowed when that is
+ * 0), 256-byte aligned.  The result of each row does not depend on M or on
+ * the other rows. */
+size_t fg_dequant_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+fg_status fg_dequant_gemm_g4(const fg_f16* X, int64_t M, const fg_q4* W,
+                             const fg_f16* bias, const fg_f16* residual,
+                             int32_t act, fg_f16* Y, void* workspace,
+                             size_t ws_bytes, fg_stream stream);
+
+/* Y = X W^T with fp16 W [N][K] and an fp32 result (the LM head against the
+ * tied token embedding).  X [M][K] fp16; Y [M][N] fp32; K % 64 == 0. */
+fg_status fg_gemm_f16_f32out(const fg_f16* X, int64_t M, const fg_f16* W,
+                             int64_t N, int64_t K, float* Y, fg_stream stream);
+
+/* ------------------------------------------------------------------ small ops */
+
+/* y = (x - mean) / sqrt(var + eps) * gamma + beta per row; mean and biased
+ * variance in fp32 (the OPT layer's pre-LayerNorm and final LayerNorm).
+ * Row r of x starts at x + r * x_ld (x_ld >= cols, x_ld % 8 == 0), so the
+ * last token of each sequence can be normalised in place; y: [rows][cols]
+ * contiguous fp16.  cols % 8 == 0, cols <= 16384. */
+fg_status fg_layernorm(const fg_f16* x, int64_t rows, int64_t cols,
+                       int64_t x_ld, const fg_f16* gamma, const fg_f16* beta,
+                       float eps, fg_f16* y, fg_stream stream);
+
+/* y[r] = e_tok[ids[r]] + e_pos[pos0 + r % T] for r in [0, ntok): the token
+ * embedding plus the learned position embedding of sequence-major rows of T
+ * tokens starting at position pos0.  ids: [ntok] int32 in [0, vocab).
+ * e_tok [vocab][h1], e_pos [npos][h1], y [ntok][h1] fp16; h1 % 8 == 0. */
+fg_status fg_embed(const int32_t* ids, int64_t ntok, int32_t T, int32_t pos0,
+                   const fg_f16* e_tok, int64_t vocab, const fg_f16* e_pos,
+                   int64_t npos, int32_t h1, fg_f16* y, fg_stream stream);
+
+/* ------------------------------------------------------------------ KV cache and attention */
+
+/* Quantise the new token's k and v (one row per sequence) into cache slot
+ * pos, per head, in groups of 64 along the head dimension (the decode-step
+ * append of "FlexGen 完全拆解", dataflow section).  qkv: [B][qkv_ld] fp16
+ * holding q | k | v of width h1 = H*d each; qkv_ld >= 3*h1, qkv_ld % 8 == 0.
+ * 0 <= pos < cap.  Bit-exact with fg_quantize_g4 on the same values. */
+fg_status fg_kv_append_g4(const fg_f16* qkv, int64_t qkv_ld,
+                          const fg_kv4* cache, int32_t pos, fg_stream stream);
+
+/* Decode attention over the 4-bit cache: for each sequence b and head h,
+ * out = sum_j softmax_j(q . k^_j / sqrt(d)) v^_j over slots j = 0..pos,
+ * with k^, v^ the dequantised cache rows.  If fuse_append != 0 the new k, v
+ * are first appended into slot pos exactly as fg_kv_append_g4 does (in the
+ * same launch).  qkv as for fg_kv_append_g4; out: [B][h1] fp16. */
+fg_status fg_decode_attn_g4(const fg_f16* qkv, int64_t qkv_ld,
+                            const fg_kv4* cache, int32_t pos,
+                            int32_t fuse_append, fg_f16* out,
+                            fg_stream stream);
+
+/* Causal prefill attention for B sequences of s prompt tokens over the fp16
+ * K, V straight from the QKV projection: out_i = sum_{j<=i}
+ * softmax_j(q_i . k_j / sqrt(d)) v_j.  qkv: [B*s][3*h1] fp16 (sequence-major
+ * rows); out: [B*s][h1] fp16.  If cache is not NULL, the K and V rows of
+ * every prompt token are also quantised into slots 0..s-1 (s <= cap,
+ * cache->B == B, H and d must match). */
+fg_status fg_prefill_attn(const fg_f16* qkv, int32_t B, int32_t s, int32_t H,
+                          int32_t d, const fg_kv4* cache, fg_f16* out,
+                          fg_stream stream);
+
+/* ------------------------------------------------------------------ layer step */
+
+/* One decoder layer for bls = p.gbs * p.k sequences of T new tokens:
+ *   h = x + OutProj(Attn(LN1(x)));  y = h + FC2(ReLU(FC1(LN2(h)))).
+ * phase FG_PHASE_PREFILL: T = s prompt tokens at positions 0..T-1 (the K/V
+ * rows are stored into slots 0..T-1).  phase FG_PHASE_DECODE: T = 1; the new
+ * token's K/V are appended at slot pos and attended over slots 0..pos.
+ * x_in, x_out: [bls*T][h1] fp16, sequence-major rows (may not alias).
+ * cache->B must equal bls.  The k GPU batches are rows / cache sequences
+ * [i*gbs, (i+1)*gbs).  workspace: device scratch of at least
+ * fg_layer_workspace_bytes(w, phase, bls, T, p) bytes, 256-byte aligned. */
+size_t fg_layer_workspace_bytes(const fg_layer* w, int32_t phase, int32_t bls,
+                                int32_t T, fg_policy p);
+fg_status fg_layer_step(const fg_layer* w, const fg_kv4* cache,
+                        const fg_f16* x_in, fg_f16* x_out, int32_t phase,
+                        int32_t T, int32_t pos, fg_policy p, void* workspace,
+                        size_t ws_bytes, fg_stream stream);
+
+/* ------------------------------------------------------------------ test knobs */
+
+/* Host-side test knobs (0 = off).  FG_KNOB_DROP_ARRIVE: the next
+ * fg_dequant_gemm_g4 launch makes its producer skip one barrier arrive, so
+ * the consumers' bounded waits expire and the launch reports
+ * FG_ERR_TIMEOUT through fg_check() instead of hanging.
+ * FG_KNOB_WAIT_NS: override the device wait limit in nanoseconds (0 =
+ * default, about 2 s). */
+enum { FG_KNOB_DROP_ARRIVE = 1, FG_KNOB_WAIT_NS = 2 };
+fg_status fg_debug_set(int32_t knob, int64_t value);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FG_H */

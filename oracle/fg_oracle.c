@@ -121,6 +121,16 @@ void or_set_num_threads(int n)
 /* low nibble of byte j and element 2j+1 in the high nibble.                  */
 /* ------------------------------------------------------------------------ */
 
+/* a < b in the IEEE total order restricted to finite values: numeric order,
+ * with -0 below +0 (so the sign of a zero minimum or maximum is defined by
+ * the values, not by where they sit in the group). */
+static int total_less(float a, float b)
+{
+    if (a < b) return 1;
+    if (a > b) return 0;
+    return signbit(a) && !signbit(b);
+}
+
 static void quantize_group(const uint16_t* x, uint8_t* codes, float* meta)
 {
     float v[OR_GROUP];
@@ -129,8 +139,8 @@ static void quantize_group(const uint16_t* x, uint8_t* codes, float* meta)
 
     float mn = v[0], mx = v[0];
     for (int i = 1; i < OR_GROUP; ++i) {
-        if (v[i] < mn) mn = v[i];
-        if (v[i] > mx) mx = v[i];
+        if (total_less(v[i], mn)) mn = v[i];
+        if (total_less(mx, v[i])) mx = v[i];
     }
     float range = mx - mn;          /* fp32 subtract */
     float scale = range / 15.0f;    /* fp32 IEEE divide, 15 = 2^4 - 1 levels */

@@ -158,6 +158,17 @@ def test_min_max_codes_and_reconstruction_bound(idx):
     assert np.all(np.abs(xg - xh) <= bound)
 
 
+def test_signed_zero_min_is_order_independent():
+    """min/max use the IEEE total order (-0 below +0): a group of zeros of
+    both signs stores min = -0 and max = +0 wherever the -0 sits."""
+    for where in (0, 17, 63):
+        x = np.zeros((1, 64), np.float16)
+        x[0, where] = np.float16(-0.0)
+        codes, meta = oracle.quantize_g4(x)
+        assert np.signbit(meta[0, 0, 0]) and meta[0, 0, 1] == 0.0
+        assert np.all(codes == 0)
+
+
 def test_monotone_codes():
     rng = np.random.default_rng(2)
     x = np.sort(rng.standard_normal((16, 64 * 8)).reshape(16, 8, 64), -1).reshape(16, -1)
