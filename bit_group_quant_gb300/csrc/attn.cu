@@ -269,6 +269,12 @@ fg_status launch_decode_t(const __half* qkv, int64_t ld, const fg_kv4* c, int32_
         if (e != cudaSuccess) return fg::cuda_error(e, "decode_attn smem attribute");
     }
     dim3 grid(c->H, c->B);
+    // algorithmic traffic: L packed K and V rows (codes + fp32 meta) per (b, h),
+    // the new k, v written back, q/k/v read and the output written
+    const double row = D / 2 + (D / 64) * 8.0;
+    const double bh = static_cast<double>(c->B) * c->H;
+    fg::TraceScope ts(FG_TRACE_ATTN_DECODE, st, 4.0 * bh * L * D,
+                      bh * (2.0 * L * row + (fuse_append ? 2.0 * row : 0.0) + 3.0 * D * 2 + D * 2));
     kern<<<grid, kDecThreads, smem, st>>>(qkv, ld, c->H, c->cap, pos, fuse_append, c->k_codes,
                                           c->v_codes, c->k_meta, c->v_meta, out);
     return fg::cuda_error(cudaGetLastError(), "decode_attn launch");
@@ -289,6 +295,9 @@ fg_status launch_prefill_attn(const __half* qkv, int32_t B, int32_t s, int32_t H
                               __half* out, cudaStream_t st) {
     if (B == 0 || s == 0) return FG_OK;
     dim3 grid(static_cast<unsigned>(cdiv(s, kPreQ)), H, B);
+    const double bh = static_cast<double>(B) * H;
+    TraceScope ts(FG_TRACE_ATTN_PREFILL, st, 2.0 * bh * s * (s + 1.0) * d,
+                  bh * s * d * 2.0 * 4.0);
     if (d == 64)
         prefill_attn_kernel<64><<<grid, 128, 0, st>>>(qkv, s, H, out);
     else

@@ -27,6 +27,20 @@ uint64_t wait_limit_ns();
 int take_drop_arrive();                    // test knob: consumed by the next GEMM launch
 int num_sms();
 
+// Tracing (fg_trace_begin / fg_trace_end): counts every launch of the class
+// and, when the class is timed, brackets the launch with a CUDA event pair.
+class TraceScope {
+  public:
+    TraceScope(int cls_bit, cudaStream_t st, double flops, double bytes);
+    ~TraceScope();
+    TraceScope(const TraceScope&) = delete;
+    TraceScope& operator=(const TraceScope&) = delete;
+
+  private:
+    int rec_ = -1;
+    cudaStream_t st_;
+};
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

@@ -377,6 +377,16 @@ fg_status run_gemm(const CUtensorMap& tmX, const CUtensorMap& tmW, GemmParams& p
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return fg::cuda_error(e, "gemm smem attribute");
     dim3 grid(plan.feat_tiles, plan.tok_tiles, plan.splits);
+    const double M = p.M, N = p.N, K = p.K;
+    // algorithmic traffic: the weight once (4-bit codes + fp32 (min, scale) per
+    // 64, or fp16), X once, Y once (+ residual, or fp32 partials / logits)
+    const double wbytes = kDequant ? N * K * 0.625 : N * K * 2.0;
+    const double ybytes = kF32Out ? M * N * 4.0
+                                  : (plan.splits > 1 ? plan.splits * M * N * 4.0
+                                                     : M * N * 2.0 * (p.residual ? 2.0 : 1.0));
+    const int cls = !kDequant ? FG_TRACE_OTHER
+                              : (p.M > 256 ? FG_TRACE_GEMM_PREFILL : FG_TRACE_GEMM_DECODE);
+    fg::TraceScope ts(cls, st, 2.0 * M * N * K, wbytes + M * K * 2.0 + ybytes);
     kern<<<grid, kThreads, smem, st>>>(tmX, tmW, p);
     return fg::cuda_error(cudaGetLastError(), "gemm launch");
 }
@@ -453,6 +463,7 @@ fg_status launch_gemm_g4(const __half* X, int64_t M, const fg_q4* W, const __hal
     const int64_t nv = M * N / 4;
     int64_t blocks = cdiv(nv, 256);
     if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
+    TraceScope ts(FG_TRACE_OTHER, st, 0.0, pl.splits * M * N * 4.0 + M * N * 4.0);
     splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
         p.partial, pl.splits, M, N, bias, residual, act, Y);
     return cuda_error(cudaGetLastError(), "splitk reduce launch");

@@ -158,6 +158,7 @@ fg_status launch_quantize_g4(const __half* x, int64_t ngroups, uint8_t* codes, f
                              cudaStream_t st) {
     if (ngroups == 0) return FG_OK;
     const int grid = grid_for(ngroups, 32);  // 32 groups per 256-thread block
+    TraceScope ts(FG_TRACE_OTHER, st, 0.0, ngroups * (128.0 + 40.0));
     quantize_g4_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), ngroups,
                                              reinterpret_cast<uint32_t*>(codes),
                                              reinterpret_cast<float2*>(meta));
@@ -168,6 +169,7 @@ fg_status launch_dequant_g4(const uint8_t* codes, const float* meta, int64_t ngr
                             __half* x, cudaStream_t st) {
     if (ngroups == 0) return FG_OK;
     const int grid = grid_for(ngroups * 8, 256);
+    TraceScope ts(FG_TRACE_OTHER, st, 0.0, ngroups * (128.0 + 40.0));
     dequant_g4_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(codes),
                                             reinterpret_cast<const float2*>(meta), ngroups,
                                             reinterpret_cast<uint4*>(x));
@@ -179,6 +181,7 @@ fg_status launch_kv_store(const __half* qkv, int64_t ld, int32_t B, int32_t T, i
     const int64_t ngroups = static_cast<int64_t>(B) * T * 2 * H * (d / 64);
     if (ngroups == 0) return FG_OK;
     const int grid = grid_for(ngroups, 32);
+    TraceScope ts(FG_TRACE_OTHER, st, 0.0, ngroups * (128.0 + 40.0));
     kv_store_kernel<<<grid, 256, 0, st>>>(qkv, ld, B, T, H, d, c->cap, slot0, c->k_codes,
                                           c->v_codes, c->k_meta, c->v_meta);
     return cuda_error(cudaGetLastError(), "kv_store launch");

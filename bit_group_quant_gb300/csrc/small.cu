@@ -131,6 +131,7 @@ fg_status launch_layernorm(const __half* x, int64_t rows, int64_t cols, int64_t 
     if (cols > static_cast<int64_t>(kLnMaxVec) * 8 * kLnThreads)
         return set_error(FG_ERR_UNSUPPORTED, "layernorm: cols %lld > %d", (long long)cols,
                          kLnMaxVec * 8 * kLnThreads);
+    TraceScope ts(FG_TRACE_OTHER, st, 0.0, rows * cols * 4.0);
     layernorm_kernel<<<static_cast<unsigned>(rows), kLnThreads, 0, st>>>(x, cols, x_ld, g, b, eps, y);
     return cuda_error(cudaGetLastError(), "layernorm launch");
 }
@@ -141,6 +142,7 @@ fg_status launch_embed(const int32_t* ids, int64_t ntok, int32_t T, int32_t pos0
     if (ntok == 0) return FG_OK;
     int64_t blocks = cdiv(ntok * (h1 / 8), 256);
     if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
+    TraceScope ts(FG_TRACE_OTHER, st, 0.0, ntok * h1 * 6.0);
     embed_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(ids, ntok, T, pos0, e_tok, e_pos,
                                                                 h1, y);
     return cuda_error(cudaGetLastError(), "embed launch");

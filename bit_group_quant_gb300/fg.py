@@ -28,7 +28,7 @@ EXPORTS = (
     "fg_dequant_g4", "fg_dequant_gemm_workspace_bytes", "fg_dequant_gemm_g4",
     "fg_gemm_f16_f32out", "fg_layernorm", "fg_embed", "fg_kv_append_g4",
     "fg_decode_attn_g4", "fg_prefill_attn", "fg_layer_workspace_bytes", "fg_layer_step",
-    "fg_debug_set",
+    "fg_debug_set", "fg_trace_begin", "fg_trace_end",
 )
 
 
@@ -62,6 +62,16 @@ class c_layer(ctypes.Structure):
                 ("ln2_g", ctypes.c_void_p), ("ln2_b", ctypes.c_void_p),
                 ("h1", ctypes.c_int32), ("H", ctypes.c_int32), ("h2", ctypes.c_int32),
                 ("ln_eps", ctypes.c_float)]
+
+
+FG_TRACE_GEMM_PREFILL, FG_TRACE_GEMM_DECODE, FG_TRACE_ATTN_DECODE, FG_TRACE_ATTN_PREFILL, \
+    FG_TRACE_OTHER = 1, 2, 4, 8, 16
+TRACE_CLASSES = ("gemm_prefill", "gemm_decode", "attn_decode", "attn_prefill", "other")
+
+
+class c_trace_stats(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_int64 * 5), ("ms", ctypes.c_double * 5),
+                ("flops", ctypes.c_double * 5), ("bytes", ctypes.c_double * 5)]
 
 
 _lock = threading.Lock()
@@ -99,6 +109,8 @@ def load(path: str = LIB_PATH):
             "fg_layer_step": ([ctypes.POINTER(c_layer), ctypes.POINTER(c_kv4), P, P, I32, I32,
                                I32, c_policy, P, SZ, P], st),
             "fg_debug_set": ([I32, I64], st),
+            "fg_trace_begin": ([I32], st),
+            "fg_trace_end": ([ctypes.POINTER(c_trace_stats)], st),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -198,6 +210,19 @@ def fg_check(stream=None):
 
 def fg_debug_set(knob, value):
     _ok(load().fg_debug_set(int(knob), int(value)))
+
+
+def fg_trace_begin(timed_mask=0):
+    _ok(load().fg_trace_begin(int(timed_mask)))
+
+
+def fg_trace_end() -> dict:
+    """Returns {class: {"launches", "ms", "flops", "bytes"}}."""
+    st = c_trace_stats()
+    _ok(load().fg_trace_end(ctypes.byref(st)))
+    return {name: {"launches": int(st.launches[i]), "ms": float(st.ms[i]),
+                   "flops": float(st.flops[i]), "bytes": float(st.bytes[i])}
+            for i, name in enumerate(TRACE_CLASSES)}
 
 
 def fg_quantize_g4(x, out: Q4 | None = None, stream=None) -> Q4:

@@ -163,7 +163,8 @@ fg_status fg_dequant_gemm_g4(const fg_f16* X, int64_t M, const fg_q4* W,
                              size_t ws_bytes, fg_stream stream);
 
 /* Y = X W^T with fp16 W [N][K] and an fp32 result (the LM head against the
- * tied token embedding).  X [M][K] fp16; Y [M][N] fp32; K % 64 == 0. */
+ * tied token embedding).  X [M][K] fp16; Y [M][N] fp32; K % 64 == 0; any
+ * N >= 1 (the vocabulary need not be a multiple of the tile). */
 fg_status fg_gemm_f16_f32out(const fg_f16* X, int64_t M, const fg_f16* W,
                              int64_t N, int64_t K, float* Y, fg_stream stream);
 
@@ -233,6 +234,34 @@ fg_status fg_layer_step(const fg_layer* w, const fg_kv4* cache,
                         const fg_f16* x_in, fg_f16* x_out, int32_t phase,
                         int32_t T, int32_t pos, fg_policy p, void* workspace,
                         size_t ws_bytes, fg_stream stream);
+
+/* ------------------------------------------------------------------ tracing */
+
+/* Kernel classes for tracing (bit mask). */
+enum {
+    FG_TRACE_GEMM_PREFILL = 1 << 0,  /* dequant GEMM launches with M > 256 rows */
+    FG_TRACE_GEMM_DECODE = 1 << 1,   /* dequant GEMM launches with M <= 256 rows */
+    FG_TRACE_ATTN_DECODE = 1 << 2,
+    FG_TRACE_ATTN_PREFILL = 1 << 3,
+    FG_TRACE_OTHER = 1 << 4,         /* quantiser, KV store, LayerNorm, embedding, LM head, reductions */
+    FG_TRACE_NCLASS = 5
+};
+
+/* Per-class totals since the last fg_trace_begin. */
+typedef struct fg_trace_stats {
+    int64_t launches[FG_TRACE_NCLASS];   /* kernel launches, counted on the host */
+    double ms[FG_TRACE_NCLASS];          /* summed device time of the timed classes */
+    double flops[FG_TRACE_NCLASS];       /* algorithmic FLOPs of the launches */
+    double bytes[FG_TRACE_NCLASS];       /* algorithmic HBM bytes of the launches */
+} fg_trace_stats;
+
+/* Start counting launches of every class and, for the classes in
+ * `timed_mask`, record a CUDA event pair around each launch on its stream.
+ * Host-side only; nothing is allocated on the device (CUDA events are
+ * created once and reused). */
+fg_status fg_trace_begin(int32_t timed_mask);
+/* Stop, wait for the recorded events and return the totals. */
+fg_status fg_trace_end(fg_trace_stats* out);
 
 /* ------------------------------------------------------------------ test knobs */
 
