@@ -1,0 +1,429 @@
+"""Benchmark: decode tokens/s of 4-bit group-quantised, block-scheduled OPT
+generation on GB300, plus the dequant-GEMM TFLOP/s and 4-bit KV-attention
+GB/s measured inside the same timed region.
+
+One step = one whole pass of the hot path over one block: prefill of bls
+prompts (embedding, every layer, final LayerNorm and LM head) followed by the
+n-1 teacher-forced decode steps.  Default workload: OPT-30B-shaped model
+(48 layers, h1 7168, 56 heads, h2 28672, vocab 50272), gbs 48 x k 3 =
+bls 144, s 512, n 32, weights and KV cache 4-bit g64, all resident in HBM.
+
+`value` = bls * (n-1) / (device time of the decode phase), summed over
+ranks over the max-over-ranks time.  Inputs (18.5 GB of weights, 33.7 GB of
+KV cache) are far larger than L2, so no flush is needed between steps.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun each rank runs an independent replica on its own GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = ("decode tokens/s at bls=144,s=512,n=32; dequant-GEMM TFLOP/s; "
+          "4-bit KV-attn GB/s")
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------
+# distributed helpers (replicas: no collective on the data path)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def reduce_scalar(x: float, op: str, device="cpu") -> float:
+    """Max or sum of one float over all ranks (identity with one process)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    rop = torch.distributed.ReduceOp.MAX if op == "max" else torch.distributed.ReduceOp.SUM
+    torch.distributed.all_reduce(t, op=rop)
+    return float(t.item())
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def aggregate(units_per_rank: float, seconds_per_rank: float, device="cpu"):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    units = reduce_scalar(units_per_rank, "sum", device)
+    secs = reduce_scalar(seconds_per_rank, "max", device)
+    return units / secs, secs
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# --------------------------------------------------------------------------
+# peaks and committed ncu traffic
+# --------------------------------------------------------------------------
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_hash(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def committed_traffic(kernel_file: str, workload: str):
+    """Per-launch DRAM bytes of the kernel from profiles/traffic.json, valid
+    only while the kernel source is unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_file + ":" + workload)
+    src = os.path.join(ROOT, "bit_group_quant_gb300", "csrc", kernel_file)
+    if not d or d.get("source_sha") != kernel_hash(src):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------
+# CPU baseline (the oracle, as it stands, on a bounded sample)
+# --------------------------------------------------------------------------
+
+def oracle_sample(wl, nseq: int, seed: int = 0, frac: int = 16):
+    """Time the oracle on a bounded sample of one decode token step: every
+    projection of one layer on a 1/frac row slice of its weight, the decode
+    attention of nseq sequences over all heads at context s+1 (cache of
+    quantised N(0,1) rows), both LayerNorms, and a 1/frac slice of the LM
+    head; the slices are scaled by frac and the layer by the layer count.
+    Returns (decode tokens/s, seconds of CPU work, threads used)."""
+    import oracle
+
+    g = synth.generator(seed)
+    h1, h2 = wl.h1, wl.h2
+    shapes = [(3 * h1, h1), (h1, h1), (h2, h1), (h1, h2)]
+    slices = []
+    for n, k in shapes:
+        w = synth.normal_f16((n // frac, k), 0.02, g).numpy()
+        x = synth.normal_f16((nseq, k), 1.0, g).numpy()
+        slices.append((x, oracle.quantize_g4(w)))
+    cache = oracle.KVCache(nseq, wl.H, wl.d, wl.s + 1)
+    rows = synth.normal_f16((2, nseq * wl.H * wl.s, wl.d), 1.0, g).numpy()
+    kc, km = oracle.quantize_g4(rows[0])
+    vc, vm = oracle.quantize_g4(rows[1])
+    cache.k_codes[:, :, :wl.s] = kc.reshape(nseq, wl.H, wl.s, -1)
+    cache.k_meta[:, :, :wl.s] = km.reshape(nseq, wl.H, wl.s, -1, 2)
+    cache.v_codes[:, :, :wl.s] = vc.reshape(nseq, wl.H, wl.s, -1)
+    cache.v_meta[:, :, :wl.s] = vm.reshape(nseq, wl.H, wl.s, -1, 2)
+    qkv = synth.normal_f16((nseq, 3 * h1), 1.0, g).numpy()
+    xh = synth.normal_f16((nseq, h1), 1.0, g).numpy()
+    e_tok = synth.normal_f16((max(wl.vocab // frac, 1), h1), 0.02, g).numpy()
+    ones, zeros = np.ones(h1, np.float16), np.zeros(h1, np.float16)
+
+    t0 = time.perf_counter()
+    for x, (codes, meta) in slices:
+        oracle.linear_g4(x, codes, meta)
+    t1 = time.perf_counter()
+    oracle.decode_attn_g4(qkv, cache, wl.s, append=True)
+    oracle.layernorm(xh, ones, zeros)
+    oracle.layernorm(xh, ones, zeros)
+    t2 = time.perf_counter()
+    oracle.linear_f16_f32out(oracle.layernorm(xh, ones, zeros), e_tok)
+    t3 = time.perf_counter()
+    layer = frac * (t1 - t0) + (t2 - t1)
+    per_token_step = wl.layers * layer + frac * (t3 - t2)
+    return nseq / per_token_step, (t3 - t0), oracle.num_threads()
+
+
+# --------------------------------------------------------------------------
+# the GPU arm
+# --------------------------------------------------------------------------
+
+def run_fg(args, ws, rank, local):
+    from bit_group_quant_gb300 import fg
+    from bit_group_quant_gb300.model import random_model
+
+    wl = synth.WORKLOADS[args.workload]
+    D = wl.decode_steps
+
+    cpu_base = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, secs, cores = oracle_sample(wl, args.cpu_seqs, frac=args.cpu_frac)
+        cpu_base = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                    "sample": "one decode token step of %d sequences at context %d: 1/%d row "
+                              "slices of the four projections and the LM head (scaled by %d), "
+                              "full attention and LayerNorms, one layer scaled to %d "
+                              "(%.1f s of CPU work)" % (args.cpu_seqs, wl.s, args.cpu_frac,
+                                                        args.cpu_frac, wl.layers, secs)}
+
+    torch.cuda.set_device(local)
+    dev = "cuda:%d" % local
+    init_dist(ws, "nccl")
+    stream = torch.cuda.current_stream()
+
+    model = random_model(wl, seed=0, device=dev)
+    g = synth.generator(1000 + rank, dev)
+    prompt = synth.token_ids((wl.bls, wl.s), wl.vocab, g, dev)
+    dec_tm = synth.token_ids((D, wl.bls), wl.vocab, g, dev)
+    logits_buf = [torch.empty((wl.bls, wl.vocab), dtype=torch.float32, device=dev)
+                  for _ in range(2)]
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        model.prefill(prompt, args.order, logits=logits_buf[0])
+        if evs:
+            evs[1].record(stream)
+        for t in range(1, D + 1):
+            model.decode_step(dec_tm[t - 1], t, wl.s, args.order, logits=logits_buf[t % 2])
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    fg.fg_check()
+
+    # ---------------- timed region (device-resident inputs)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    fg.fg_trace_begin(fg.FG_TRACE_GEMM_PREFILL | fg.FG_TRACE_GEMM_DECODE |
+                      fg.FG_TRACE_ATTN_DECODE | fg.FG_TRACE_ATTN_PREFILL)
+    for k in range(args.steps):
+        step(evs[k])
+    torch.cuda.synchronize()
+    trace = fg.fg_trace_end()
+    barrier()
+    clk = clocks.stop()
+    fg.fg_check()
+    t_pre = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+    t_dec = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+    value, t_dec_max = aggregate(wl.bls * D * args.steps, t_dec, dev)
+    gen_value, t_all_max = aggregate(wl.bls * wl.n * args.steps, t_pre + t_dec, dev)
+
+    # ---------------- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_prompt = prompt.cpu().pin_memory()
+        h_dec = dec_tm.cpu().pin_memory()
+        h_logits = torch.empty((wl.bls, wl.vocab), dtype=torch.float32).pin_memory()
+        d_prompt = torch.empty_like(prompt)
+        d_dec = torch.empty_like(dec_tm)
+        e2e_dec = 0.0
+        barrier()
+        torch.cuda.synchronize()
+        for k in range(args.steps):
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            d_prompt.copy_(h_prompt, non_blocking=True)
+            model.prefill(d_prompt, args.order, logits=logits_buf[0])
+            e1.record(stream)
+            d_dec.copy_(h_dec, non_blocking=True)
+            for t in range(1, D + 1):
+                lg = model.decode_step(d_dec[t - 1], t, wl.s, args.order,
+                                       logits=logits_buf[t % 2])
+                h_logits.copy_(lg, non_blocking=True)
+            e2.record(stream)
+            torch.cuda.synchronize()
+            e2e_dec += e1.elapsed_time(e2) / 1e3
+        e2e_value, _ = aggregate(wl.bls * D * args.steps, e2e_dec, dev)
+        e2e = {"value": e2e_value, "unit": UNIT,
+               "h2d_bytes_per_step": int(h_prompt.numel() * 4 + h_dec.numel() * 4),
+               "d2h_bytes_per_step": int(D * h_logits.numel() * 4),
+               "note": "decode phase timed from the H2D copy of the step's token ids to the "
+                       "D2H copy of every decode step's logits into pinned host memory"}
+        fg.fg_check()
+
+    if rank != 0:
+        return None
+
+    peaks, peak_kind = load_peaks()
+    gp = trace["gemm_prefill"]
+    gd = trace["gemm_decode"]
+    ad = trace["attn_decode"]
+    ap = trace["attn_prefill"]
+    tflops = lambda c: c["flops"] / (c["ms"] / 1e3) / 1e12 if c["ms"] > 0 else None
+    gbs = lambda c: c["bytes"] / (c["ms"] / 1e3) / 1e9 if c["ms"] > 0 else None
+    # The dominant kernel of the step is the prefill dequant-GEMM (tensor-bound);
+    # it runs inside a seconds-long step, so the sustained cuBLAS figure is the peak.
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    achieved = tflops(gp)
+    launches = sum(c["launches"] for c in trace.values())
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_all_max / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
+        "data": "synthetic",
+        "config": {"workload": "%s-shaped: %d layers, h1 %d, %d heads, h2 %d, vocab %d; "
+                               "gbs %d x k %d = bls %d, s %d, n %d (%d decode steps); "
+                               "weights and KV 4-bit g64 in HBM"
+                               % (wl.name, wl.layers, wl.h1, wl.H, wl.h2, wl.vocab, wl.gbs,
+                                  wl.k, wl.bls, wl.s, wl.n, D),
+                   "order": args.order, "parallelism": "replicas" if ws > 1 else "single",
+                   "l2": "inputs larger than L2 (weights %.1f GB, KV %.1f GB)"
+                         % (sum(L.nbytes_q4 for L in model.stack.layers) / 1e9,
+                            sum(c.nbytes for c in model.stack.caches) / 1e9)},
+        "generation_tokens_per_s": gen_value,
+        "gemm_tflops": {"prefill": tflops(gp), "decode": tflops(gd)},
+        "attn_gbs": {"decode_4bit": gbs(ad)},
+        "phase_ms_per_step": {"prefill": t_pre / args.steps * 1e3,
+                              "decode": t_dec / args.steps * 1e3},
+        "kernel_ms_per_step": {k: c["ms"] / args.steps for k, c in trace.items()},
+        "roofline": {"kernel": "gemm_tc_kernel<dequant> (prefill launches)", "bound": "tensor",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak if achieved else None,
+                     "peak_source": "%s bf16_tflops_sustained (fp16 dense rate = bf16)" % peak_kind,
+                     "traffic": committed_traffic("gemm.cu", wl.name),
+                     "launches": gp["launches"],
+                     "avg_launch_ms": gp["ms"] / max(gp["launches"], 1)},
+        "decode_roofline": {
+            "gemm": {"bound": "tensor", "achieved": tflops(gd), "unit": "TFLOP/s",
+                     "frac": tflops(gd) / peak if tflops(gd) else None},
+            "attn": {"bound": "hbm", "achieved": gbs(ad), "unit": "GB/s",
+                     "peak": peaks["hbm_gbs"],
+                     "frac": gbs(ad) / peaks["hbm_gbs"] if gbs(ad) else None}},
+        "prefill_attn_tflops": tflops(ap),
+        "cpu_baseline": cpu_base,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    return line
+
+
+def run_reference(args, ws, rank):
+    """The oracle timed on this host's cores: each step is a bounded sample."""
+    if rank != 0:
+        return None
+    wl = synth.WORKLOADS[args.workload]
+    for _ in range(args.warmup):
+        oracle_sample(wl, args.ref_seqs, seed=1, frac=args.ref_frac)
+    vals, secs = [], 0.0
+    cores = 1
+    for k in range(args.steps):
+        v, s, cores = oracle_sample(wl, args.ref_seqs, seed=2 + k, frac=args.ref_frac)
+        vals.append(v)
+        secs += s
+    value = len(vals) / sum(1.0 / v for v in vals)
+    sample = ("per step: one decode token step of %d sequences at context %d: 1/%d row slices "
+              "of the four projections and the LM head (scaled by %d), full attention and "
+              "LayerNorms, one layer scaled to %d layers (%.1f s of CPU work per step)"
+              % (args.ref_seqs, wl.s, args.ref_frac, args.ref_frac, wl.layers,
+                 secs / max(args.steps, 1)))
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "%s-shaped, bls %d, s %d, n %d" % (wl.name, wl.bls, wl.s, wl.n)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="fg", choices=["fg", "reference"])
+    ap.add_argument("--workload", default="opt-30b", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--order", default="block", choices=["block", "zigzag"])
+    ap.add_argument("--cpu-seqs", type=int, default=8)
+    ap.add_argument("--ref-seqs", type=int, default=2)
+    ap.add_argument("--cpu-frac", type=int, default=1)
+    ap.add_argument("--ref-frac", type=int, default=4)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, ws, rank)
+    else:
+        line = run_fg(args, ws, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
