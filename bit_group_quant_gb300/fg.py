@@ -28,7 +28,7 @@ EXPORTS = (
     "fg_dequant_g4", "fg_dequant_gemm_workspace_bytes", "fg_dequant_gemm_g4",
     "fg_gemm_f16_f32out", "fg_layernorm", "fg_embed", "fg_kv_append_g4",
     "fg_decode_attn_g4", "fg_prefill_attn", "fg_layer_workspace_bytes", "fg_layer_step",
-    "fg_debug_set", "fg_trace_begin", "fg_trace_end",
+    "fg_debug_set", "fg_trace_begin", "fg_trace_end", "fg_dequant_gemm_g4_noalloc",
 )
 
 
@@ -100,6 +100,7 @@ def load(path: str = LIB_PATH):
             "fg_dequant_gemm_workspace_bytes": ([I64, I64, I64], SZ),
             "fg_dequant_gemm_g4": ([P, I64, ctypes.POINTER(c_q4), P, P, I32, P, P, SZ, P], st),
             "fg_gemm_f16_f32out": ([P, I64, P, I64, I64, P, P], st),
+            "fg_dequant_gemm_g4_noalloc": ([P, I64, ctypes.POINTER(c_q4), P, P, I32, P, P], st),
             "fg_layernorm": ([P, I64, I64, I64, P, P, F, P, P], st),
             "fg_embed": ([P, I64, I32, I32, P, I64, P, I64, I32, P, P], st),
             "fg_kv_append_g4": ([P, I64, ctypes.POINTER(c_kv4), I32, P], st),
@@ -260,6 +261,24 @@ def fg_dequant_gemm_g4(X, W: Q4, bias=None, residual=None, act=FG_ACT_NONE, Y=No
     _ok(load().fg_dequant_gemm_g4(_ptr(X), M, ctypes.byref(c), _ptr(bias), _ptr(residual),
                                   int(act), _ptr(Y), _ptr(workspace), ws_bytes,
                                   _stream(stream)))
+    return Y
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def fg_dequant_gemm_g4_noalloc(X, W: Q4, bias=None, residual=None, act=FG_ACT_NONE, Y=None,
+                               stream=None):
+    """fg_dequant_gemm_g4 without a workspace argument, for callers that must
+    not allocate device memory (the K-split scratch is a fixed 16 MiB array
+    inside libfg).  Y must be passed in by such callers; it is created here
+    only for convenience when omitted."""
+    M = X.shape[0]
+    if Y is None:
+        Y = torch.empty((M, W.rows), dtype=torch.float16, device=X.device)
+    c = W.c()
+    _ok(load().fg_dequant_gemm_g4_noalloc(_ptr(X), M, ctypes.byref(c), _ptr(bias),
+                                          _ptr(residual), int(act), _ptr(Y), _stream(stream)))
     return Y
 
 

@@ -162,6 +162,28 @@ fg_status fg_dequant_gemm_g4(const fg_f16* X, int64_t M, const fg_q4* W,
                              int32_t act, fg_f16* Y, void* workspace,
                              size_t ws_bytes, fg_stream stream);
 
+/* The same computation as fg_dequant_gemm_g4, for callers that must not
+ * allocate device memory: a plugin inside a host program that owns the
+ * device-memory budget through its own pool and forbids other allocations,
+ * or a latency-critical loop where cudaMalloc/cudaFree would synchronise the
+ * device.  No counterpart in the paper: it exists only for such callers.
+ * Inputs and outputs are as for fg_dequant_gemm_g4 (the caller still
+ * passes X, W, bias, residual and Y); the K-split scratch comes from a
+ * fixed 16 MiB device array inside the library (held on every GPU that
+ * loads it until the process exits), so no workspace is passed and nothing
+ * is allocated.  Shapes whose K-split scratch,
+ * fg_dequant_gemm_workspace_bytes(M, N, K), exceeds 16 MiB are rejected
+ * with FG_ERR_WORKSPACE before any launch.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  All
+ * calls share the array and it keeps the last call's contents (no call
+ * relies on them: every partial sum read is written earlier in the same
+ * call); calls that overlap on the GPU -- on different streams of one
+ * device -- race on it and must be serialised by the caller. */
+fg_status fg_dequant_gemm_g4_noalloc(const fg_f16* X, int64_t M, const fg_q4* W,
+                                     const fg_f16* bias, const fg_f16* residual,
+                                     int32_t act, fg_f16* Y, fg_stream stream);
+
 /* Y = X W^T with fp16 W [N][K] and an fp32 result (the LM head against the
  * tied token embedding).  X [M][K] fp16; Y [M][N] fp32; K % 64 == 0; any
  * N >= 1 (the vocabulary need not be a multiple of the tile). */
