@@ -369,6 +369,108 @@ def run_fg(args, ws, rank, local):
     return line
 
 
+# --------------------------------------------------------------------------
+# kernel micro-benchmarks: one kernel on one shape (ncu captures), and the
+# OPT-175B single-layer sweep
+# --------------------------------------------------------------------------
+
+def _time_launches(fn, iters, stream):
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(iters):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters / 1e3
+
+
+def gemm_case(M, N, K, iters, dev, seed=0):
+    """One dequant-GEMM launch shape; returns (seconds, TFLOP/s, GB/s)."""
+    from bit_group_quant_gb300 import fg
+    g = synth.generator(seed, dev)
+    q = fg.fg_quantize_g4(synth.normal_f16((N, K), 0.02, g, dev))
+    x = synth.normal_f16((M, K), 1.0, g, dev)
+    y = torch.empty((M, N), dtype=torch.float16, device=dev)
+    ws_n = fg.fg_dequant_gemm_workspace_bytes(M, N, K)
+    ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev)
+    fn = lambda: fg.fg_dequant_gemm_g4(x, q, Y=y, workspace=ws)
+    sec = _time_launches(fn, iters, torch.cuda.current_stream())
+    fg.fg_check()
+    flops = 2.0 * M * N * K
+    bytes_ = 0.625 * N * K + 2.0 * M * K + 2.0 * M * N
+    return sec, flops / sec / 1e12, bytes_ / sec / 1e9
+
+
+def attn_case(B, H, d, L, iters, dev, seed=0):
+    """One decode-attention launch over a full 4-bit cache of L rows
+    (fused append at slot L-1); returns (seconds, GB/s)."""
+    from bit_group_quant_gb300 import fg
+    g = synth.generator(seed, dev)
+    cache = fg.KV4.empty(B, H, d, L, dev, zero=False)
+    rows = synth.normal_f16((B * H * L, d), 1.0, g, dev)
+    kq = fg.fg_quantize_g4(rows)
+    cache.k_codes.copy_(kq.codes.view_as(cache.k_codes))
+    cache.k_meta.copy_(kq.meta.view_as(cache.k_meta))
+    vq = fg.fg_quantize_g4(synth.normal_f16((B * H * L, d), 1.0, g, dev))
+    cache.v_codes.copy_(vq.codes.view_as(cache.v_codes))
+    cache.v_meta.copy_(vq.meta.view_as(cache.v_meta))
+    del rows, kq, vq
+    qkv = synth.normal_f16((B, 3 * H * d), 1.0, g, dev)
+    out = torch.empty((B, H * d), dtype=torch.float16, device=dev)
+    fn = lambda: fg.fg_decode_attn_g4(qkv, cache, L - 1, fuse_append=True, out=out)
+    sec = _time_launches(fn, iters, torch.cuda.current_stream())
+    fg.fg_check()
+    row = d / 2 + (d / 64) * 8
+    bytes_ = B * H * (2.0 * L * row + 2 * row + 8.0 * d)
+    return sec, bytes_ / sec / 1e9
+
+
+def run_micro(args):
+    torch.cuda.set_device(0)
+    dev = "cuda:0"
+    peaks, kind = load_peaks()
+    if args.micro == "gemm":
+        sec, tf, gb = gemm_case(args.M, args.N, args.K, args.iters, dev)
+        return {"micro": "dequant_gemm", "M": args.M, "N": args.N, "K": args.K,
+                "ms": sec * 1e3, "tflops": tf, "gbs": gb,
+                "frac_tensor": tf / peaks["bf16_tflops"], "peak_source": kind + " bf16_tflops"}
+    if args.micro == "attn":
+        sec, gb = attn_case(args.B, args.H, args.d, args.L, args.iters, dev)
+        return {"micro": "decode_attn_g4", "B": args.B, "H": args.H, "d": args.d, "L": args.L,
+                "ms": sec * 1e3, "gbs": gb, "frac_hbm": gb / peaks["hbm_gbs"],
+                "peak_source": kind + " hbm_gbs"}
+    # OPT-175B single-layer sweep: dequant-GEMM at bls in {32,144,256,512} for
+    # the four projection shapes, decode attention at bls 144 for three contexts
+    h1, H, h2 = synth.OPT175B_H1, synth.OPT175B_H, synth.OPT175B_H2
+    shapes = {"qkv": (3 * h1, h1), "out": (h1, h1), "fc1": (h2, h1), "fc2": (h1, h2)}
+    gemm = {}
+    for bls in synth.SWEEP_GEMM_BLS:
+        tot_f = tot_s = tot_b = 0.0
+        per = {}
+        for name, (N, K) in shapes.items():
+            sec, tf, gb = gemm_case(bls, N, K, args.iters, dev)
+            per[name] = {"ms": sec * 1e3, "tflops": tf, "gbs": gb}
+            tot_f += 2.0 * bls * N * K
+            tot_b += 0.625 * N * K + 2.0 * bls * (K + N)
+            tot_s += sec
+        tf = tot_f / tot_s / 1e12
+        gb = tot_b / tot_s / 1e9
+        bound = "hbm" if bls < 144 else "tensor"
+        frac = gb / peaks["hbm_gbs"] if bound == "hbm" else tf / peaks["bf16_tflops"]
+        gemm[str(bls)] = {"layer_ms": tot_s * 1e3, "tflops": tf, "gbs": gb, "bound": bound,
+                          "frac": frac, "per_projection": per}
+    attn = {}
+    for L in synth.SWEEP_ATTN_CTX:
+        sec, gb = attn_case(synth.SWEEP_ATTN_BLS, H, h1 // H, L, args.iters, dev)
+        attn[str(L)] = {"ms": sec * 1e3, "gbs": gb, "frac_hbm": gb / peaks["hbm_gbs"]}
+    return {"sweep": "opt-175b layer: h1 12288, 96 heads of 128, h2 49152",
+            "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tflops")}, "peak_source": kind,
+            "dequant_gemm": gemm, "decode_attn_bls144": attn}
+
+
 def run_reference(args, ws, rank):
     """The oracle timed on this host's cores: each step is a bounded sample."""
     if rank != 0:
@@ -413,8 +515,21 @@ def main(argv=None):
     ap.add_argument("--ref-frac", type=int, default=4)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--micro", choices=["gemm", "attn", "sweep175b"], default=None,
+                    help="time one kernel shape (or the OPT-175B layer sweep) instead")
+    ap.add_argument("--M", type=int, default=4096)
+    ap.add_argument("--N", type=int, default=28672)
+    ap.add_argument("--K", type=int, default=7168)
+    ap.add_argument("--B", type=int, default=144)
+    ap.add_argument("--H", type=int, default=56)
+    ap.add_argument("--d", type=int, default=128)
+    ap.add_argument("--L", type=int, default=513)
+    ap.add_argument("--iters", type=int, default=10)
     args = ap.parse_args(argv)
     ws, rank, local = dist_env()
+    if args.micro:
+        print(json.dumps(run_micro(args)), flush=True)
+        return
     if args.impl == "reference":
         line = run_reference(args, ws, rank)
     else:
