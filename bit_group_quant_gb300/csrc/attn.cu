@@ -28,36 +28,75 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Exact dequantised value, as a float: fp16(fma(code, scale, min)).
-__device__ __forceinline__ float deq(uint32_t code, float2 m) {
-    return __half2float(__float2half_rn(__fmaf_rn(static_cast<float>(code), m.y, m.x)));
+// ---------------------------------------------------------------------------
+// Decode attention over the 4-bit cache.
+//
+// For a cached row with codes c, group min m and scale s (per 64 dims):
+//   q . k^  = sum_g [ m_g * Q_g + s_g * sum_{i in g} q_i c_i ],  Q_g = sum_{i in g} q_i
+//   sum_j p_j v^_j[i] = sum_j p_j m_{j,g} + sum_j (p_j s_{j,g}) c_{j,i}
+// so (min, scale) apply once per key and group, and the code dot products run
+// on the tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate) with the
+// codes encoded exactly as fp16 1 + c/16 (one shift and one LOP3 per pair of
+// codes); sum (1 + c/16) x = sum x + (1/16) sum c x removes the offset.
+//
+// One CTA (4 warps) per (head, sequence); warps take 16-key tiles in turn.
+// Pass 1: scores of all L keys into shared memory.  Then the exact maximum
+// and p_j = exp(score_j - max).  Pass 2: the V sums.  K and V are each read
+// once from HBM (16-byte / 32-byte coalesced lane loads).
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// One CTA per (head, sequence).  Shared memory: scores[L] then the partial
-// output table [R][D].
+// half2(1 + c_e/16, 1 + c_{e+4}/16) from nibbles e and e+4 of w (e in 0..3).
+__device__ __forceinline__ uint32_t nib_pair(uint32_t w, int e) {
+    const uint32_t sh = e == 0 ? (w << 6) : e == 1 ? (w << 2) : e == 2 ? (w >> 2) : (w >> 6);
+    return (sh & 0x03C003C0u) | 0x3C003C00u;
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t ldg32(const uint8_t* p) {
+    return *reinterpret_cast<const uint32_t*>(p);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
     const __half* __restrict__ qkv, int64_t ld, int32_t H, int32_t cap, int32_t pos,
     int32_t fuse_append, uint8_t* k_codes, uint8_t* v_codes, float* k_meta, float* v_meta,
     __half* __restrict__ out) {
-    constexpr int GPR = D / 64;          // groups per head row
-    constexpr int TPR = D / 8;           // threads per V row (8 dims each)
-    constexpr int R = kDecThreads / TPR; // V rows in flight per pass
+    constexpr int G = D / 64;            // groups per head row
+    constexpr int RB = D / 2;            // code bytes per row
+    constexpr int WPT = D / 32;          // code words per lane per row in pass 1
+    constexpr int NX = 2 * WPT;          // pass-1 MMAs per 16 keys
+    constexpr int NWARP = kDecThreads / 32;
     extern __shared__ float dsm[];
-    __shared__ float qf[D];
-    __shared__ float red[kDecThreads / 32];
+    __shared__ float qsum[G];
+    __shared__ float red[NWARP];
+    __shared__ float part[NWARP][D];
+    __shared__ float part_s[NWARP][2][2];   // per warp, per group: sum p m, sum p'
 
     const int h = blockIdx.x, b = blockIdx.y;
     const int L = pos + 1;
     const int64_t h1 = static_cast<int64_t>(H) * D;
     const int64_t row0 = (static_cast<int64_t>(b) * H + h) * cap;  // cache row of slot 0
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
     float* sc = dsm;
-    float* part = dsm + ((L + 3) & ~3);
 
-    if (fuse_append && threadIdx.x < 32) {
-        const int lane = threadIdx.x, grp = lane >> 3, lane8 = lane & 7;
-        const bool valid = grp < 2 * GPR;
-        const int is_v = grp / GPR, gi = grp % GPR;
+    if (fuse_append && warp == 0) {
+        const int grp = lane >> 3, lane8 = lane & 7;
+        const bool valid = grp < 2 * G;
+        const int is_v = grp / G, gi = grp % G;
         float v[8];
         if (valid) {
             const uint4 raw = *reinterpret_cast<const uint4*>(
@@ -77,52 +116,111 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
         const uint32_t packed = quantize8(v, mn, scale);
         if (valid) {
             const int64_t row = row0 + pos;
-            uint8_t* cdst = (is_v ? v_codes : k_codes) + row * (D / 2) + gi * 32;
+            uint8_t* cdst = (is_v ? v_codes : k_codes) + row * RB + gi * 32;
             reinterpret_cast<uint32_t*>(cdst)[lane8] = packed;
             if (lane8 == 0) {
-                float* mdst = (is_v ? v_meta : k_meta) + (row * GPR + gi) * 2;
+                float* mdst = (is_v ? v_meta : k_meta) + (row * G + gi) * 2;
                 *reinterpret_cast<float2*>(mdst) = make_float2(mn, scale);
             }
         }
     }
-    for (int t = threadIdx.x; t < D; t += kDecThreads)
-        qf[t] = __half2float(qkv[b * ld + static_cast<int64_t>(h) * D + t]);
+    const __half* qrow = qkv + b * ld + static_cast<int64_t>(h) * D;
+    if (warp == 1) {   // per-group sums of q (fp32)
+        float s0 = 0.0f, s1 = 0.0f;
+        for (int i = lane; i < D; i += 32) {
+            const float qv = __half2float(qrow[i]);
+            if (i < 64) s0 += qv; else s1 += qv;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+            s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        }
+        if (lane == 0) {
+            qsum[0] = s0;
+            if (G > 1) qsum[G - 1] = s1;
+        }
+    }
+    // q as the B operand of the pass-1 MMAs: lane (g, t) owns code words
+    // WPT*t .. WPT*t + WPT-1 of a row (dims 8 WPT t ..); MMA x uses word x/2,
+    // nibble pairs (2h, 2h+4) and (2h+1, 2h+5) with h = x % 2.  Column n = g of
+    // B holds q restricted to group g (columns >= G are zero), so the MMA sums
+    // each group separately.
+    uint32_t qb[NX][2];
+    {
+        const int my_grp = (WPT * t * 8) / 64;
+        const bool use = g < G && g == my_grp;
+#pragma unroll
+        for (int x = 0; x < NX; ++x) {
+            const int base = 8 * (WPT * t + (x >> 1)) + 2 * (x & 1);
+            const float q0 = use ? __half2float(qrow[base]) : 0.0f;
+            const float q4 = use ? __half2float(qrow[base + 4]) : 0.0f;
+            const float q1 = use ? __half2float(qrow[base + 1]) : 0.0f;
+            const float q5 = use ? __half2float(qrow[base + 5]) : 0.0f;
+            qb[x][0] = pack_h2(q0, q4);
+            qb[x][1] = pack_h2(q1, q5);
+        }
+    }
     __syncthreads();
 
-    const float scale = __fdiv_rn(1.0f, __fsqrt_rn(static_cast<float>(D)));
-    // Scores: one cache row per thread, dot product in ascending dimension.
+    const float attn_scale = __fdiv_rn(1.0f, __fsqrt_rn(static_cast<float>(D)));
+    const float Q0 = qsum[0], Q1 = qsum[G - 1];
+    const int ntile = (L + 15) >> 4;
+
+    // ---------------- pass 1: scores
     float lmax = -CUDART_INF_F;
-    for (int j = threadIdx.x; j < L; j += kDecThreads) {
-        const uint4* kc = reinterpret_cast<const uint4*>(k_codes + (row0 + j) * (D / 2));
-        const float2* km = reinterpret_cast<const float2*>(k_meta + (row0 + j) * GPR * 2);
-        float dot = 0.0f;
+    for (int kt = warp; kt < ntile; kt += NWARP) {
+        const int ja = min(kt * 16 + g, L - 1), jb = min(kt * 16 + g + 8, L - 1);
+        const uint8_t* ra = k_codes + (row0 + ja) * RB + t * (WPT * 4);
+        const uint8_t* rb = k_codes + (row0 + jb) * RB + t * (WPT * 4);
+        uint32_t wa[WPT], wb[WPT];
+        if (WPT == 4) {
+            const uint4 va = *reinterpret_cast<const uint4*>(ra);
+            const uint4 vb = *reinterpret_cast<const uint4*>(rb);
+            wa[0] = va.x; wa[1] = va.y; wa[WPT > 2 ? 2 : 0] = va.z; wa[WPT > 3 ? 3 : 0] = va.w;
+            wb[0] = vb.x; wb[1] = vb.y; wb[WPT > 2 ? 2 : 0] = vb.z; wb[WPT > 3 ? 3 : 0] = vb.w;
+        } else {
+            const uint2 va = *reinterpret_cast<const uint2*>(ra);
+            const uint2 vb = *reinterpret_cast<const uint2*>(rb);
+            wa[0] = va.x; wa[1] = va.y;
+            wb[0] = vb.x; wb[1] = vb.y;
+        }
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int g = 0; g < GPR; ++g) {
-            const float2 m = km[g];
+        for (int x = 0; x < NX; ++x) {
+            const int e = 2 * (x & 1);
+            mma16816(acc, nib_pair(wa[x >> 1], e), nib_pair(wb[x >> 1], e),
+                     nib_pair(wa[x >> 1], e + 1), nib_pair(wb[x >> 1], e + 1), qb[x][0], qb[x][1]);
+        }
+        if (t == 0) {
+            // acc: (key g, group 0), (key g, group 1), (key g+8, group 0), (key g+8, group 1)
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const uint4 raw = kc[g * 2 + u];
-                const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                for (int wi = 0; wi < 4; ++wi) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int dim = g * 64 + u * 32 + wi * 8 + e;
-                        dot = __fadd_rn(dot, __fmul_rn(qf[dim], deq((w4[wi] >> (4 * e)) & 0xF, m)));
+            for (int half = 0; half < 2; ++half) {
+                const int j = kt * 16 + g + 8 * half;
+                if (j < L) {
+                    const float* km = k_meta + (row0 + j) * G * 2;
+                    float dot;
+                    if (G == 2) {
+                        const float4 m = *reinterpret_cast<const float4*>(km);
+                        dot = m.x * Q0 + 16.0f * m.y * (acc[2 * half] - Q0) +
+                              m.z * Q1 + 16.0f * m.w * (acc[2 * half + 1] - Q1);
+                    } else {
+                        const float2 m = *reinterpret_cast<const float2*>(km);
+                        dot = m.x * Q0 + 16.0f * m.y * (acc[2 * half] - Q0);
                     }
+                    const float s = dot * attn_scale;
+                    sc[j] = s;
+                    lmax = fmaxf(lmax, s);
                 }
             }
         }
-        const float s = __fmul_rn(dot, scale);
-        sc[j] = s;
-        lmax = fmaxf(lmax, s);
     }
     lmax = warp_max(lmax);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = lmax;
+    if (lane == 0) red[warp] = lmax;
     __syncthreads();
     float mx = red[0];
 #pragma unroll
-    for (int i = 1; i < kDecThreads / 32; ++i) mx = fmaxf(mx, red[i]);
+    for (int i = 1; i < NWARP; ++i) mx = fmaxf(mx, red[i]);
     __syncthreads();
     float lsum = 0.0f;
     for (int j = threadIdx.x; j < L; j += kDecThreads) {
@@ -131,32 +229,98 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
         lsum += p;
     }
     lsum = warp_sum(lsum);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = lsum;
+    if (lane == 0) red[warp] = lsum;
     __syncthreads();
     float l = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kDecThreads / 32; ++i) l += red[i];
+    for (int i = 0; i < NWARP; ++i) l += red[i];
 
-    // Weighted V sum: TPR threads per row, 8 dims each; R rows per pass.
-    const int r = threadIdx.x / TPR, c8 = threadIdx.x % TPR;
-    float acc[8];
+    // ---------------- pass 2: V.  MMA e (nibble e of every code word) has rows
+    // = dims (row g: word g, row g+8: word 8+g) and k = 16 keys paired in
+    // registers; B column n = g holds p_j * s_{j,g} (fp16) for group g.
+    float accv[8][4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-    for (int j = r; j < L; j += R) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(v_codes + (row0 + j) * (D / 2) + c8 * 4);
-        const float2 m = reinterpret_cast<const float2*>(v_meta + (row0 + j) * GPR * 2)[c8 / 8];
-        const float p = sc[j];
+    for (int e = 0; e < 8; ++e) accv[e][0] = accv[e][1] = accv[e][2] = accv[e][3] = 0.0f;
+    float s_pm = 0.0f, s_p2 = 0.0f;   // this lane's keys: sum p m, sum p' (group g)
+    const bool gown = g < G;
+    for (int kt = warp; kt < ntile; kt += NWARP) {
+        const int j0 = kt * 16;
+        int keys[4] = {j0 + 2 * t, j0 + 2 * t + 1, j0 + 2 * t + 8, j0 + 2 * t + 9};
+        uint32_t bw[2] = {0u, 0u};
+        {
+            float pp[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], __fmul_rn(p, deq((w >> (4 * e)) & 0xF, m)));
+            for (int u = 0; u < 4; ++u) {
+                const bool ok = keys[u] < L;
+                const float p = ok ? sc[keys[u]] : 0.0f;
+                float pv = 0.0f;
+                if (gown && ok) {
+                    const float2 m = *reinterpret_cast<const float2*>(
+                        v_meta + ((row0 + keys[u]) * G + g) * 2);
+                    pv = p * m.y;
+                    s_pm += p * m.x;
+                }
+                pp[u] = pv;
+            }
+            bw[0] = pack_h2(pp[0], pp[1]);
+            bw[1] = pack_h2(pp[2], pp[3]);
+            const float2 r0 = __half22float2(*reinterpret_cast<const __half2*>(&bw[0]));
+            const float2 r1 = __half22float2(*reinterpret_cast<const __half2*>(&bw[1]));
+            s_p2 += (r0.x + r0.y) + (r1.x + r1.y);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) keys[u] = min(keys[u], L - 1);
+        // code words: word g (dims 8g..8g+7) and, for D = 128, word 8+g
+        uint32_t w0[4], w1[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint8_t* r = v_codes + (row0 + keys[u]) * RB;
+            w0[u] = ldg32(r + 4 * g);
+            w1[u] = (D == 128) ? ldg32(r + 32 + 4 * g) : 0u;
+        }
+        // (key pair, word) -> PRMT so each 16-bit half holds one key's nibbles
+        const uint32_t lo0 = __byte_perm(w0[0], w0[1], 0x5410), hi0 = __byte_perm(w0[0], w0[1], 0x7632);
+        const uint32_t lo2 = __byte_perm(w0[2], w0[3], 0x5410), hi2 = __byte_perm(w0[2], w0[3], 0x7632);
+        const uint32_t lo1 = __byte_perm(w1[0], w1[1], 0x5410), hi1 = __byte_perm(w1[0], w1[1], 0x7632);
+        const uint32_t lo3 = __byte_perm(w1[2], w1[3], 0x5410), hi3 = __byte_perm(w1[2], w1[3], 0x7632);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t a0 = nib_pair(e < 4 ? lo0 : hi0, e & 3);
+            const uint32_t a2 = nib_pair(e < 4 ? lo2 : hi2, e & 3);
+            const uint32_t a1 = (D == 128) ? nib_pair(e < 4 ? lo1 : hi1, e & 3) : 0u;
+            const uint32_t a3 = (D == 128) ? nib_pair(e < 4 ? lo3 : hi3, e & 3) : 0u;
+            mma16816(accv[e], a0, a1, a2, a3, bw[0], bw[1]);
+        }
     }
+    // group sums of this warp: reduce over the 4 lanes (g, t) of each group
 #pragma unroll
-    for (int e = 0; e < 8; ++e) part[r * D + c8 * 8 + e] = acc[e];
+    for (int o = 1; o < 4; o <<= 1) {
+        s_pm += __shfl_xor_sync(0xffffffffu, s_pm, o);
+        s_p2 += __shfl_xor_sync(0xffffffffu, s_p2, o);
+    }
+    if (t == 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            part[warp][8 * g + e] = accv[e][0];                 // group 0 dims x p'(group 0)
+            if (D == 128) part[warp][64 + 8 * g + e] = accv[e][3];  // group 1 dims x p'(group 1)
+        }
+        if (gown) {
+            part_s[warp][g][0] = s_pm;
+            part_s[warp][g][1] = s_p2;
+        }
+    }
     __syncthreads();
-    for (int t = threadIdx.x; t < D; t += kDecThreads) {
-        float o = 0.0f;
+    for (int i = threadIdx.x; i < D; i += kDecThreads) {
+        const int grp = i >> 6;
+        float dsum = 0.0f, pm = 0.0f, p2 = 0.0f;
 #pragma unroll
-        for (int rr = 0; rr < R; ++rr) o += part[rr * D + t];
-        out[b * h1 + static_cast<int64_t>(h) * D + t] = __float2half_rn(__fdiv_rn(o, l));
+        for (int w = 0; w < NWARP; ++w) {
+            dsum += part[w][i];
+            pm += part_s[w][grp][0];
+            p2 += part_s[w][grp][1];
+        }
+        const float o = (pm + 16.0f * (dsum - p2)) / l;
+        out[b * h1 + static_cast<int64_t>(h) * D + i] = __float2half_rn(o);
     }
 }
 
@@ -261,7 +425,7 @@ template <int D>
 fg_status launch_decode_t(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
                           int32_t fuse_append, __half* out, cudaStream_t st) {
     const int L = pos + 1;
-    const size_t smem = sizeof(float) * (((L + 3) & ~3) + kDecThreads * 8);
+    const size_t smem = sizeof(float) * ((L + 3) & ~3);
     auto kern = decode_attn_kernel<D>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -12,13 +12,15 @@
 // At decode, nt = bls: each weight tile is fetched from HBM and dequantised
 // exactly once per block, which is the block schedule's weight reuse.
 //
-// Warp roles (192 threads): warp 0 = TMA producer (activations and packed
+// Warp roles (320 threads): warp 0 = TMA producer (activations and packed
 // codes into a ring of shared-memory stages); warp 1 = TMEM allocator and
-// the single MMA-issuing thread; warps 2-5 = dequantisers (one weight row per
-// thread: 32 code bytes from shared memory + (min, scale) -> 64 fp16 written
-// in the 128-byte-swizzled K-major layout the MMA descriptor reads), then
-// the epilogue (tcgen05.ld of the accumulator, bias / ReLU / residual, fp16
-// store) -- or fp32 partial sums when K is split.
+// the single MMA-issuing thread; warps 2-9 = dequantisers (two threads per
+// weight row, each 16 code bytes from shared memory + (min, scale) -> 32
+// fp16 written in the 128-byte-swizzled K-major layout the MMA descriptor
+// reads), then the epilogue (tcgen05.ld of the accumulator, bias / ReLU /
+// residual, fp16 store) -- or fp32 partial sums when K is split.
+// CTAs walk the output tiles in groups of 16 feature tiles x all token
+// tiles, so weight and activation tiles are reused from L2.
 //
 // Every mbarrier wait is bounded; a wait that expires flags the CTA to stop,
 // records a timeout in the device status word, waits for its own copies and
@@ -33,7 +35,9 @@ namespace {
 
 using namespace fgd;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kDeqThreads = 256;
+constexpr int kRasterGroup = 16;     // feature tiles per rasterisation group
 constexpr int kTileF = 128;          // output features per CTA (MMA M)
 constexpr int kChunk = 64;           // k per stage: one 128-byte swizzle row of fp16
 constexpr uint32_t kABytes = kTileF * kChunk * 2;   // 16 KB
@@ -50,6 +54,7 @@ struct GemmParams {
     float* partial;           // [splits][M][N] fp32 when splits > 1
     int M, N, K;
     int nt;                   // activation rows per tile (MMA N)
+    int feat_tiles, tok_tiles;
     int kchunks;              // K / 64
     int kc_per_split;
     int act;
@@ -114,8 +119,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto c_smem = [&](int s) { return b_smem(s) + b_bytes; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int feat0 = blockIdx.x * kTileF;
-    const int tok0 = blockIdx.y * p.nt;
+    // grouped rasterisation: within a group of kRasterGroup feature tiles the
+    // feature tile varies fastest, then the token tile
+    int feat_tile, tok_tile;
+    {
+        const int id = blockIdx.x;
+        const int per_group = kRasterGroup * p.tok_tiles;
+        const int grp = id / per_group;
+        const int f0 = grp * kRasterGroup;
+        const int gf = min(kRasterGroup, p.feat_tiles - f0);
+        const int r = id - grp * per_group;
+        feat_tile = f0 + r % gf;
+        tok_tile = r / gf;
+    }
+    const int feat0 = feat_tile * kTileF;
+    const int tok0 = tok_tile * p.nt;
     const int kc0 = blockIdx.z * p.kc_per_split;
     const int kc1 = min(p.kchunks, kc0 + p.kc_per_split);
     const int nk = kc1 - kc0;
@@ -125,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(deq_bar(s), 128);
+            mbar_init(deq_bar(s), kDeqThreads);
             mbar_init(empty_bar(s), 1);
         }
         mbar_init(acc_bar, 1);
@@ -202,10 +220,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(acc_bar);  // also on abort: lets the epilogue drain the MMAs in flight
         }
     } else {
-        const int dt = threadIdx.x - 64;  // 0..127
+        const int dt = threadIdx.x - 64;  // 0..255
         if (kDequant) {
-            // ---------------- dequantisers: thread dt owns weight row dt of the tile
-            const int n = feat0 + dt;
+            // ---------------- dequantisers: thread dt owns half hf of weight row rw
+            const int rw = dt >> 1, hf = dt & 1;
+            const int n = feat0 + rw;
             const bool nvalid = n < p.N;
             const float2* mrow = p.meta + static_cast<int64_t>(n) * p.kchunks + kc0;
             float2 ring[4];
@@ -230,15 +249,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const __half2 s2 = __float2half2_rn(mm.y);
                     const __half2 m2 = __float2half2_rn(mm.x);
-                    const uint8_t* crow = base_ptr + (c_smem(s) - base) + dt * 32;
-                    const uint4 w0 = *reinterpret_cast<const uint4*>(crow);
-                    const uint4 w1 = *reinterpret_cast<const uint4*>(crow + 16);
-                    const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                    uint8_t* arow = base_ptr + (a_smem(s) - base) + dt * 128;
+                    const uint4 w = *reinterpret_cast<const uint4*>(
+                        base_ptr + (c_smem(s) - base) + rw * 32 + hf * 16);
+                    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+                    uint8_t* arow = base_ptr + (a_smem(s) - base) + rw * 128;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 0; c < 4; ++c) {
+                        const int chunk = hf * 4 + c;
                         const uint4 v = dequant8(words[c], s2, m2);
-                        *reinterpret_cast<uint4*>(arow + ((c ^ (dt & 7)) << 4)) = v;
+                        *reinterpret_cast<uint4*>(arow + ((chunk ^ (rw & 7)) << 4)) = v;
                     }
                     fence_proxy_async_smem();
                     mbar_arrive(deq_bar(s));
@@ -251,13 +270,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) report(p.status, fg::kDevTimeout);
         tc_fence_after();
         const int q = warp & 3;               // TMEM lane quarter this warp may read
+        const int colhalf = (warp - 2) >> 2;  // two warps per quarter split the columns
         const int row = q * 32 + lane;
         const int n = feat0 + row;
         const bool live = ok && !*abort_flag;
         float bias = 0.0f;
         if (!kF32Out && live && p.bias != nullptr && n < p.N && gridDim.z == 1)
             bias = __half2float(p.bias[n]);
-        for (int c0 = 0; c0 < p.nt; c0 += 16) {
+        for (int c0 = 16 * colhalf; c0 < p.nt; c0 += 32) {
             uint32_t r[16];
             tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, r);
             tmem_wait_ld();
@@ -376,7 +396,9 @@ fg_status run_gemm(const CUtensorMap& tmX, const CUtensorMap& tmW, GemmParams& p
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return fg::cuda_error(e, "gemm smem attribute");
-    dim3 grid(plan.feat_tiles, plan.tok_tiles, plan.splits);
+    dim3 grid(plan.feat_tiles * plan.tok_tiles, 1, plan.splits);
+    p.feat_tiles = plan.feat_tiles;
+    p.tok_tiles = plan.tok_tiles;
     const double M = p.M, N = p.N, K = p.K;
     // algorithmic traffic: the weight once (4-bit codes + fp32 (min, scale) per
     // 64, or fp16), X once, Y once (+ residual, or fp32 partials / logits)
