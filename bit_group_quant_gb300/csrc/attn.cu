@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
             wb[0] = vb.x; wb[1] = vb.y;
         }
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        __syncwarp();   // mma.sync is .aligned: reconverge after last round's lane-0 work
 #pragma unroll
         for (int x = 0; x < NX; ++x) {
             const int e = 2 * (x & 1);
@@ -283,6 +284,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
         const uint32_t lo2 = __byte_perm(w0[2], w0[3], 0x5410), hi2 = __byte_perm(w0[2], w0[3], 0x7632);
         const uint32_t lo1 = __byte_perm(w1[0], w1[1], 0x5410), hi1 = __byte_perm(w1[0], w1[1], 0x7632);
         const uint32_t lo3 = __byte_perm(w1[2], w1[3], 0x5410), hi3 = __byte_perm(w1[2], w1[3], 0x7632);
+        __syncwarp();   // mma.sync is .aligned: reconverge after the per-key loads above
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const uint32_t a0 = nib_pair(e < 4 ? lo0 : hi0, e & 3);

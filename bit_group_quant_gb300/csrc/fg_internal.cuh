@@ -68,6 +68,7 @@ struct GemmPlan {
     int tok_tiles;
     int feat_tiles;  // ceil(N / 128)
     int splits;      // K splits (grid.z); > 1 only when tok_tiles == 1
+    int kc_per_split;  // K chunks (of 64) per split, a multiple of 4
     size_t ws_bytes; // fp32 partial sums when splits > 1
 };
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K);
@@ -139,6 +140,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Same, for long waits of warps that have nothing else to do: backs off with
+// __nanosleep so the spinning leaves issue slots to the other warps of its
+// sub-partition.  Never stops early on an abort flag (used for drains).
+__device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        __nanosleep(200);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > limit_ns) return false;
+    }
+}
+
 // ---- TMA (bulk tensor copies, no multicast)
 __device__ __forceinline__ void prefetch_tmap(const void* tm) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
@@ -151,6 +165,40 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tm, int x,
         "l"(tm), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
+// Multicast variant: the box lands at the same shared-memory offset in every
+// CTA of the cluster named in `mask`, completing bytes on each one's mbarrier
+// at the same offset.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tm, int x, int y,
+                                               uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(tm), "r"(x), "r"(y), "r"(bar), "h"(mask)
+        : "memory");
+}
+
+// ---- thread-block clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -191,6 +239,15 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+// Arrive once on the mbarrier at the same offset in every CTA of `mask`
+// when all previously issued tcgen05 ops of this thread have completed.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(mask)
         : "memory");
 }
 // 32 lanes x 32 bit, 16 consecutive columns per thread.

@@ -12,15 +12,22 @@
 // At decode, nt = bls: each weight tile is fetched from HBM and dequantised
 // exactly once per block, which is the block schedule's weight reuse.
 //
-// Warp roles (320 threads): warp 0 = TMA producer (activations and packed
-// codes into a ring of shared-memory stages); warp 1 = TMEM allocator and
-// the single MMA-issuing thread; warps 2-9 = dequantisers (two threads per
-// weight row, each 16 code bytes from shared memory + (min, scale) -> 32
-// fp16 written in the 128-byte-swizzled K-major layout the MMA descriptor
-// reads), then the epilogue (tcgen05.ld of the accumulator, bias / ReLU /
-// residual, fp16 store) -- or fp32 partial sums when K is split.
-// CTAs walk the output tiles in groups of 16 feature tiles x all token
-// tiles, so weight and activation tiles are reused from L2.
+// Clusters of c = 1, 2 or 4 CTAs (consecutive feature tiles, one token tile)
+// share each activation tile: every CTA loads 1/c of it and multicasts the
+// slice to the whole cluster, so the activations cross L2 once per cluster
+// instead of once per CTA.
+//
+// Warp roles (352 threads): warp 0 = TMA producer of the weight side (packed
+// codes, 4 K-chunks per 128-byte-swizzled box, or fp16 A tiles); warp 2 =
+// TMA producer of this CTA's activation slices; warp 1 = TMEM allocator and
+// the single MMA-issuing thread; warps 3-10 = dequantisers in four groups of
+// two, group g owning K chunks g, g+4, ... (two weight rows per thread: 32
+// code bytes + (min, scale) -> 64 fp16 each, written in the 128-byte-swizzled
+// K-major layout the MMA descriptor reads), then the epilogue (tcgen05.ld of
+// the accumulator, bias / ReLU / residual, fp16 store) -- or fp32 partial sums
+// when K is split.  Tiles are visited in groups of 16 feature tiles x all
+// token tiles, and each group of 4 feature tiles starts its K walk at its own
+// offset, so L2 sees neither re-reads nor hot spots.
 //
 // Every mbarrier wait is bounded; a wait that expires flags the CTA to stop,
 // records a timeout in the device status word, waits for its own copies and
@@ -35,15 +42,29 @@ namespace {
 
 using namespace fgd;
 
-constexpr int kThreads = 320;
-constexpr int kDeqThreads = 256;
+constexpr int kThreads = 416;        // 13 warps
+constexpr int kDeqWarps = 8;         // warps 3,4,6,7,8,10,11,12 (none on sub-partition 1)
+constexpr int kDeqGroups = 4;        // groups of 2 warps; group g owns chunks i = g (mod 4)
 constexpr int kRasterGroup = 16;     // feature tiles per rasterisation group
+constexpr int kRotBlock = 4;         // feature tiles sharing one K-walk offset
 constexpr int kTileF = 128;          // output features per CTA (MMA M)
-constexpr int kChunk = 64;           // k per stage: one 128-byte swizzle row of fp16
-constexpr uint32_t kABytes = kTileF * kChunk * 2;   // 16 KB
-constexpr uint32_t kCBytes = kTileF * kChunk / 2;   // 4 KB of packed codes
-constexpr int kMaxStages = 8;
+constexpr int kChunk = 64;           // k per A/B stage: one 128-byte swizzle row of fp16
+constexpr int kCodeSpan = 4;         // K chunks per codes box (128 code bytes per row)
+constexpr uint32_t kABytes = kTileF * kChunk * 2;                // 16 KB
+constexpr uint32_t kCBytes = kTileF * kChunk / 2 * kCodeSpan;    // 16 KB of packed codes
+constexpr int kCStages = 3;          // codes ring, at most (12 K chunks ahead)
+constexpr int kMaxStages = 8;        // A+B stage ring
+constexpr int kMaxBars = 2 * (kCStages + kMaxStages) + 1;
 constexpr int kSmemLimit = 227 * 1024;
+static_assert(kDeqGroups == kCodeSpan, "one chunk of every codes box per dequant group");
+// A parity wait on an mbarrier can only tell the current phase from the one
+// before it, so no thread may start waiting for a phase two ahead of the
+// barrier.  A dequant group jumps kDeqGroups chunks at a time; its previous
+// chunk guarantees the stage it waits for is at most one phase behind only if
+// the stage ring has at least kDeqGroups stages.  (With fewer, a group can
+// pass a wait early, overwrite a stage still being read and over-arrive on its
+// barrier.)  The host never launches the dequant kernel with fewer stages.
+constexpr int kMinStagesDq = kDeqGroups;
 
 struct GemmParams {
     const float2* meta;       // [N][K/64] (min, scale); dequant mode
@@ -55,18 +76,15 @@ struct GemmParams {
     int M, N, K;
     int nt;                   // activation rows per tile (MMA N)
     int feat_tiles, tok_tiles;
+    int cluster;              // CTAs per cluster sharing the activation tile
     int kchunks;              // K / 64
-    int kc_per_split;
+    int kc_per_split;         // multiple of kCodeSpan
     int act;
-    int stages;
+    int ns, sc;               // ring depths (A+B stages, codes boxes)
     int* status;
     unsigned long long wait_ns;
     int drop_arrive;
 };
-
-__device__ __forceinline__ uint32_t stage_bytes(int nt, bool dq) {
-    return kABytes + static_cast<uint32_t>(nt) * 128u + (dq ? kCBytes : 0u);
-}
 
 // 8 codes (one 32-bit word, element 0 in the lowest nibble) -> 8 fp16
 // m + c*s as four half2 words in element order.  (1024 + c) is exact in fp16
@@ -95,32 +113,71 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2, __half2 m2) {
     return r;
 }
 
+// Dequantiser index 0..7 of a warp (-1 for other warps).  Sub-partition 1
+// (warps 1, 5, 9) is left to the single MMA-issuing thread during the
+// mainloop: every instruction on its path is latency-critical.
+__device__ __forceinline__ int deq_index(int w) {
+    switch (w) {
+        case 3: return 0;
+        case 4: return 1;
+        case 6: return 2;
+        case 7: return 3;
+        case 8: return 4;
+        case 10: return 5;
+        case 11: return 6;
+        case 12: return 7;
+        default: return -1;
+    }
+}
+
+// Shared-memory carve-up, all offsets from a 1024-aligned base:
+//   stage ring [ns][A 16 KB | B nt*128 B]   (both 128B-swizzled K-major MMA
+//                                            operands; one full and one empty
+//                                            barrier per stage)
+//   codes ring [sc][16 KB]                  (packed codes of 4 K chunks)
+//   barriers, TMEM address slot, abort flag
+struct Smem {
+    uint32_t base, st0, c0, bars;
+    int ns, sc;
+    uint32_t b_bytes, st_bytes;
+    // stage s = [A: 16 KB][B: nt*128 B]
+    __device__ uint32_t a(int s) const { return st0 + static_cast<uint32_t>(s) * st_bytes; }
+    __device__ uint32_t b(int s) const { return a(s) + kABytes; }
+    __device__ uint32_t c(int s) const { return c0 + static_cast<uint32_t>(s) * kCBytes; }
+    __device__ uint32_t full(int s) const { return bars + 8u * s; }
+    __device__ uint32_t empty(int s) const { return bars + 8u * (ns + s); }
+    __device__ uint32_t c_full(int s) const { return bars + 8u * (2 * ns + s); }
+    __device__ uint32_t c_empty(int s) const { return bars + 8u * (2 * ns + sc + s); }
+    __device__ uint32_t acc() const { return bars + 8u * (2 * ns + 2 * sc); }
+    __device__ uint32_t end() const { return acc() + 8u; }
+};
+
 template <bool kDequant, bool kF32Out>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t* const base_ptr = smem_raw + (base - raw);
-
-    const int S = p.stages;
-    const uint32_t b_bytes = static_cast<uint32_t>(p.nt) * 128u;
-    const uint32_t sbytes = stage_bytes(p.nt, kDequant);
-    const uint32_t bars = base + static_cast<uint32_t>(S) * sbytes;
-    auto full_bar = [&](int s) { return bars + 8u * s; };
-    auto deq_bar = [&](int s) { return bars + 8u * (S + s); };
-    auto empty_bar = [&](int s) { return bars + 8u * (2 * S + s); };
-    const uint32_t acc_bar = bars + 8u * (3 * S);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + S * sbytes + 8 * (3 * S + 1));
+    Smem sm;
+    sm.base = (raw + 1023u) & ~1023u;
+    sm.ns = p.ns;
+    sm.sc = kDequant ? p.sc : 0;
+    sm.b_bytes = static_cast<uint32_t>(p.nt) * 128u;
+    sm.st_bytes = kABytes + sm.b_bytes;
+    sm.st0 = sm.base;
+    sm.c0 = sm.st0 + sm.ns * sm.st_bytes;
+    sm.bars = sm.c0 + sm.sc * kCBytes;
+    uint8_t* const gen = smem_raw - raw;   // generic pointer = gen + shared address
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gen + sm.end());
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    auto a_smem = [&](int s) { return base + static_cast<uint32_t>(s) * sbytes; };
-    auto b_smem = [&](int s) { return a_smem(s) + kABytes; };
-    auto c_smem = [&](int s) { return b_smem(s) + b_bytes; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ccount = p.cluster;
+    const uint32_t crank = cluster_ctarank();
+    const uint16_t cmask = static_cast<uint16_t>((1u << ccount) - 1u);
     // grouped rasterisation: within a group of kRasterGroup feature tiles the
-    // feature tile varies fastest, then the token tile
+    // feature tile varies fastest, then the token tile (a cluster is c
+    // consecutive feature tiles of one token tile)
     int feat_tile, tok_tile;
     {
         const int id = blockIdx.x;
@@ -137,25 +194,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kc0 = blockIdx.z * p.kc_per_split;
     const int kc1 = min(p.kchunks, kc0 + p.kc_per_split);
     const int nk = kc1 - kc0;
+    // Each block of kRotBlock feature tiles walks its K chunks from its own
+    // offset (whole codes boxes), so the CTAs sharing an activation tile do
+    // not all fetch the same chunk at once.  The offset depends on the
+    // feature tile only: the summation order of every output -- hence its
+    // value -- does not depend on M, the cluster size or the other rows.
+    const int nbox = nk / kCodeSpan;
+    const int rot = (nk % kCodeSpan == 0 && nbox > 0)
+                        ? kCodeSpan * static_cast<int>((static_cast<long long>(feat_tile / kRotBlock) * 37) % nbox)
+                        : 0;
+    auto chunk_at = [&](int i) { return kc0 + (i + rot) % nk; };
     const uint32_t ncols = p.nt <= 32 ? 32u : (p.nt <= 64 ? 64u : (p.nt <= 128 ? 128u : 256u));
     const uint64_t lim = p.wait_ns;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(deq_bar(s), kDeqThreads);
-            mbar_init(empty_bar(s), 1);
+        for (int s = 0; s < sm.ns; ++s) {
+            // full: the activation producer's arrive (+ B bytes), and either
+            // the 2 dequant warps owning the chunk or the fp16 A producer (+ A bytes)
+            mbar_init(sm.full(s), 1 + (kDequant ? kDeqWarps / kDeqGroups : 1));
+            // empty: one MMA commit from every CTA of the cluster (frees the
+            // local A and the multicast B of the stage)
+            mbar_init(sm.empty(s), ccount);
         }
-        mbar_init(acc_bar, 1);
+        for (int s = 0; s < sm.sc; ++s) {
+            mbar_init(sm.c_full(s), 1);
+            mbar_init(sm.c_empty(s), kDeqWarps);   // every dequant warp reads one chunk per box
+        }
+        mbar_init(sm.acc(), 1);
         // A wait that expired earlier (status not yet cleared by fg_check)
-        // makes every later CTA skip its work instead of waiting again.
+        // makes every later cluster skip its work instead of waiting again.
         *abort_flag = (p.status != nullptr && *reinterpret_cast<volatile int*>(p.status) != 0);
         fence_mbar_init();
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmW);
     }
     __syncthreads();
-    if (*abort_flag) return;  // uniform across the CTA: nothing allocated yet
+    // Every barrier of every CTA in the cluster exists before any multicast.
+    cluster_sync_all();
+    {
+        // the skip decision of rank 0 holds for the whole cluster
+        const uint32_t f0 = ld_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), 0));
+        if (f0 != 0) {
+            cluster_sync_all();   // nobody reads rank 0's flag after it leaves
+            return;               // uniform across the cluster: nothing issued yet
+        }
+    }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), ncols);
         tmem_relinquish();
@@ -165,120 +248,226 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    auto fail = [&]() {
+        *abort_flag = 1;
+        report(p.status, fg::kDevTimeout);
+    };
+
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer
+            // ---------------- weight-side TMA producer
+            if (kDequant) {
+                // one box = 128 rows x 128 code bytes = 4 K chunks
+                const int nboxes = (nk + kCodeSpan - 1) / kCodeSpan;
+                int issued_last[kCStages];
+                for (int s = 0; s < kCStages; ++s) issued_last[s] = -1;
+                const int SC = sm.sc;
+                int s = 0;
+                uint32_t ph = 0;
+                for (int t = 0; t < nboxes; ++t, s = (s + 1 == SC) ? 0 : s + 1,
+                         ph ^= (s == 0) ? 1u : 0u) {
+                    if (!mbar_wait(sm.c_empty(s), ph ^ 1u, abort_flag, lim)) {
+                        fail();
+                        break;
+                    }
+                    if (p.drop_arrive && t == 0) continue;  // test knob: never arm box 0
+                    mbar_arrive_expect_tx(sm.c_full(s), kCBytes);
+                    tma_load_2d(sm.c(s), &tmW, chunk_at(kCodeSpan * t) * (kChunk / 2), feat0,
+                                sm.c_full(s));
+                    issued_last[s] = t;
+                }
+                for (int j = 0; j < SC; ++j)   // no copy may land after this CTA leaves
+                    if (issued_last[j] >= 0)
+                        mbar_wait(sm.c_full(j), (issued_last[j] / SC) & 1, nullptr, lim);
+            } else {
+                int issued_last[kMaxStages];
+                for (int s = 0; s < kMaxStages; ++s) issued_last[s] = -1;
+                const int NS = sm.ns;
+                int s = 0;
+                uint32_t ph = 0;
+                for (int i = 0; i < nk; ++i, s = (s + 1 == NS) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
+                    if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag, lim)) {
+                        fail();
+                        break;
+                    }
+                    mbar_arrive_expect_tx(sm.full(s), kABytes);
+                    tma_load_2d(sm.a(s), &tmW, chunk_at(i) * kChunk, feat0, sm.full(s));
+                    issued_last[s] = i;
+                }
+                for (int j = 0; j < NS; ++j)
+                    if (issued_last[j] >= 0)
+                        mbar_wait(sm.full(j), (issued_last[j] / NS) & 1, nullptr, lim);
+            }
+        }
+    } else if (warp == 2) {
+        if (lane == 0) {
+            // ---------------- activation TMA producer: this CTA's 1/c slice of
+            // each B tile, multicast to every CTA of the cluster
+            const int srows = p.nt / ccount;
+            const uint32_t soff = crank * static_cast<uint32_t>(srows) * 128u;
             int issued_last[kMaxStages];
-            for (int s = 0; s < S; ++s) issued_last[s] = -1;
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % S;
-                const uint32_t ph = (i / S) & 1;
-                if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, lim)) {
-                    *abort_flag = 1;
-                    report(p.status, fg::kDevTimeout);
+            for (int s = 0; s < kMaxStages; ++s) issued_last[s] = -1;
+            const int NS = sm.ns;
+            int s = 0;
+            uint32_t ph = 0;
+            for (int i = 0; i < nk; ++i, s = (s + 1 == NS) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
+                if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag, lim)) {
+                    fail();
                     break;
                 }
-                if (p.drop_arrive && i == 0) continue;  // test knob: never arm stage 0
-                const uint32_t bytes = b_bytes + (kDequant ? kCBytes : kABytes);
-                mbar_arrive_expect_tx(full_bar(s), bytes);
-                const int kc = kc0 + i;
-                tma_load_2d(b_smem(s), &tmX, kc * kChunk, tok0, full_bar(s));
-                if (kDequant)
-                    tma_load_2d(c_smem(s), &tmW, kc * (kChunk / 2), feat0, full_bar(s));
-                else
-                    tma_load_2d(a_smem(s), &tmW, kc * kChunk, feat0, full_bar(s));
+                mbar_arrive_expect_tx(sm.full(s), sm.b_bytes);
+                tma_load_2d_mc(sm.b(s) + soff, &tmX, chunk_at(i) * kChunk,
+                               tok0 + static_cast<int>(crank) * srows, sm.full(s), cmask);
                 issued_last[s] = i;
             }
-            // Never leave with copies in flight into this CTA's shared memory.
-            for (int s = 0; s < S; ++s)
-                if (issued_last[s] >= 0)
-                    mbar_wait(full_bar(s), (issued_last[s] / S) & 1, nullptr, lim);
+            // no copy may land after this CTA leaves: wait for this stage's
+            // last phase (its completion needs every slice, ours included)
+            for (int j = 0; j < NS; ++j)
+                if (issued_last[j] >= 0)
+                    mbar_wait(sm.full(j), (issued_last[j] / NS) & 1, nullptr, lim);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer
+            // The issue loop is kept minimal: it shares its sub-partition with
+            // busy warps, so every instruction on this path costs many cycles.
+            // Ring positions advance incrementally; descriptors are built once
+            // and advanced by adding encoded byte offsets (address >> 4) to the
+            // start-address field (no carry: shared addresses < 2^18).
             const uint32_t idesc = idesc_f16_f32(kTileF, p.nt);
+            const int NS = sm.ns;
+            const uint64_t ad0 = sw128_desc(sm.a(0)), bd0 = sw128_desc(sm.b(0));
+            const uint32_t step = sm.st_bytes >> 4;
+            uint32_t fb = sm.full(0), eb = sm.empty(0), off = 0, ph = 0;
+            int s = 0;
             for (int i = 0; i < nk; ++i) {
-                const int s = i % S;
-                const uint32_t ph = (i / S) & 1;
-                bool ok = mbar_wait(full_bar(s), ph, abort_flag, lim);
-                if (ok && kDequant) ok = mbar_wait(deq_bar(s), ph, abort_flag, lim);
-                if (!ok) {
-                    *abort_flag = 1;
-                    report(p.status, fg::kDevTimeout);
+                if (!mbar_wait(fb, ph, abort_flag, lim)) {
+                    fail();
                     break;
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kChunk / 16; ++kk) {
-                    const uint64_t ad = sw128_desc(a_smem(s) + kk * 32);
-                    const uint64_t bd = sw128_desc(b_smem(s) + kk * 32);
-                    mma_f16(tmem, ad, bd, idesc, (i | kk) != 0 ? 1u : 0u);
+                for (int kk = 0; kk < kChunk / 16; ++kk)
+                    mma_f16(tmem, ad0 + off + 2 * kk, bd0 + off + 2 * kk, idesc,
+                            (i | kk) != 0 ? 1u : 0u);
+                mma_commit_mc(eb, cmask);   // frees the stage (A here, B cluster-wide)
+                if (++s == NS) {
+                    s = 0;
+                    ph ^= 1u;
+                    off = 0;
+                    fb = sm.full(0);
+                    eb = sm.empty(0);
+                } else {
+                    off += step;
+                    fb += 8u;
+                    eb += 8u;
                 }
-                mma_commit(empty_bar(s));
             }
-            mma_commit(acc_bar);  // also on abort: lets the epilogue drain the MMAs in flight
+            mma_commit(sm.acc());  // also on abort: lets the epilogue drain the MMAs in flight
         }
     } else {
-        const int dt = threadIdx.x - 64;  // 0..255
-        if (kDequant) {
-            // ---------------- dequantisers: thread dt owns half hf of weight row rw
-            const int rw = dt >> 1, hf = dt & 1;
-            const int n = feat0 + rw;
-            const bool nvalid = n < p.N;
-            const float2* mrow = p.meta + static_cast<int64_t>(n) * p.kchunks + kc0;
-            float2 ring[4];
+        const int dqi = deq_index(warp);
+        if (kDequant && dqi >= 0) {
+            // ---------------- dequantisers: group dg (2 warps) owns chunks
+            // i = dg, dg + 4, ... (chunk dg of every codes box); thread r0 of
+            // the group owns weight rows r0 and r0 + 64.  Four chunks are in
+            // flight at once, one per group.
+            const int dg = dqi >> 1, r0 = (dqi & 1) * 32 + lane;
+            const int n0 = feat0 + r0, n1 = n0 + 64;
+            const bool v0 = n0 < p.N, v1 = n1 < p.N;
+            const float2* mrow0 = p.meta + static_cast<int64_t>(n0) * p.kchunks;
+            const float2* mrow1 = p.meta + static_cast<int64_t>(n1) * p.kchunks;
+            const int nmine = nk > dg ? (nk - dg + kDeqGroups - 1) / kDeqGroups : 0;
+            constexpr int kRing = 8;
+            float2 ring0[kRing], ring1[kRing];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                ring[j] = (nvalid && j < nk) ? __ldg(mrow + j) : make_float2(0.f, 0.f);
+            for (int j = 0; j < kRing; ++j) {
+                const int kc = j < nmine ? chunk_at(dg + j * kDeqGroups) : 0;
+                ring0[j] = (v0 && j < nmine) ? __ldg(mrow0 + kc) : make_float2(0.f, 0.f);
+                ring1[j] = (v1 && j < nmine) ? __ldg(mrow1 + kc) : make_float2(0.f, 0.f);
+            }
+            // this chunk's 32 code bytes of a row are 16-byte units 2*dg and
+            // 2*dg+1 of the 128-byte row, stored at unit ^ (row % 8)
+            const uint32_t u0 = ((2u * dg) ^ (r0 & 7)) << 4, u1 = ((2u * dg + 1) ^ (r0 & 7)) << 4;
+            const int NS = sm.ns;
+            int sc = 0, sa = dg % NS;       // chunk i = dg + 4*it: codes box it, stage i % NS
+            uint32_t pc = 0, pa = (dg / NS) & 1;
             bool stop = false;
-            for (int i0 = 0; i0 < nk && !stop; i0 += 4) {
+            for (int i0 = 0; i0 < nmine && !stop; i0 += kRing) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int i = i0 + j;
-                    if (i >= nk || stop) break;
-                    const float2 mm = ring[j];
-                    if (nvalid && i + 4 < nk) ring[j] = __ldg(mrow + i + 4);
-                    const int s = i % S;
-                    const uint32_t ph = (i / S) & 1;
-                    if (!mbar_wait(full_bar(s), ph, abort_flag, lim)) {
-                        *abort_flag = 1;
-                        report(p.status, fg::kDevTimeout);
+                for (int j = 0; j < kRing; ++j) {
+                    const int it = i0 + j;
+                    if (it >= nmine || stop) break;
+                    const float2 mm0 = ring0[j], mm1 = ring1[j];
+                    if (it + kRing < nmine) {
+                        const int kc = chunk_at(dg + (it + kRing) * kDeqGroups);
+                        if (v0) ring0[j] = __ldg(mrow0 + kc);
+                        if (v1) ring1[j] = __ldg(mrow1 + kc);
+                    }
+                    // every lane waits; the outcome is made warp-uniform so no
+                    // lane can leave the loop while others sit in __syncwarp
+                    if (!__all_sync(0xffffffffu, mbar_wait(sm.c_full(sc), pc, abort_flag, lim))) {
+                        fail();
                         stop = true;
                         break;
                     }
-                    const __half2 s2 = __float2half2_rn(mm.y);
-                    const __half2 m2 = __float2half2_rn(mm.x);
-                    const uint4 w = *reinterpret_cast<const uint4*>(
-                        base_ptr + (c_smem(s) - base) + rw * 32 + hf * 16);
-                    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-                    uint8_t* arow = base_ptr + (a_smem(s) - base) + rw * 128;
+                    const uint8_t* c0p = gen + sm.c(sc) + r0 * 128;
+                    const uint8_t* c1p = c0p + 64 * 128;
+                    const uint4 wa0 = *reinterpret_cast<const uint4*>(c0p + u0);
+                    const uint4 wb0 = *reinterpret_cast<const uint4*>(c0p + u1);
+                    const uint4 wa1 = *reinterpret_cast<const uint4*>(c1p + u0);
+                    const uint4 wb1 = *reinterpret_cast<const uint4*>(c1p + u1);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sm.c_empty(sc));
+                    if (!__all_sync(0xffffffffu, mbar_wait(sm.empty(sa), pa ^ 1u, abort_flag, lim))) {
+                        fail();
+                        stop = true;
+                        break;
+                    }
+                    const __half2 s20 = __float2half2_rn(mm0.y), m20 = __float2half2_rn(mm0.x);
+                    const __half2 s21 = __float2half2_rn(mm1.y), m21 = __float2half2_rn(mm1.x);
+                    const uint32_t w0[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wb0.x, wb0.y, wb0.z, wb0.w};
+                    const uint32_t w1[8] = {wa1.x, wa1.y, wa1.z, wa1.w, wb1.x, wb1.y, wb1.z, wb1.w};
+                    uint8_t* a0p = gen + sm.a(sa) + r0 * 128;
+                    uint8_t* a1p = a0p + 64 * 128;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int chunk = hf * 4 + c;
-                        const uint4 v = dequant8(words[c], s2, m2);
-                        *reinterpret_cast<uint4*>(arow + ((chunk ^ (rw & 7)) << 4)) = v;
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t off = (c ^ (r0 & 7)) << 4;
+                        *reinterpret_cast<uint4*>(a0p + off) = dequant8(w0[c], s20, m20);
+                        *reinterpret_cast<uint4*>(a1p + off) = dequant8(w1[c], s21, m21);
                     }
                     fence_proxy_async_smem();
-                    mbar_arrive(deq_bar(s));
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sm.full(sa));
+                    // next chunk of this group: codes box +1, stage +4 (mod NS)
+                    if (++sc == sm.sc) { sc = 0; pc ^= 1u; }
+                    sa += kDeqGroups;
+                    while (sa >= NS) { sa -= NS; pa ^= 1u; }
                 }
             }
         }
-        // ---------------- epilogue (the accumulator barrier is also the drain
-        // of every MMA issued, so it does not stop early on the abort flag)
-        const bool ok = mbar_wait(acc_bar, 0, nullptr, lim);
-        if (!ok) report(p.status, fg::kDevTimeout);
+        if (warp > 10) goto done;   // warps 11 and 12 only dequantise
+        {
+        // ---------------- epilogue, warps 3..10 (the accumulator barrier is
+        // also the drain of every MMA issued, so it does not stop early on the
+        // abort flag)
+        // Lanes may leave the backed-off wait at different times: __all_sync
+        // makes the outcome uniform and reconverges the warp before the
+        // .sync.aligned TMEM loads below.
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_sleepy(sm.acc(), 0, lim));
+        if (!ok && lane == 0) report(p.status, fg::kDevTimeout);
         tc_fence_after();
-        const int q = warp & 3;               // TMEM lane quarter this warp may read
-        const int colhalf = (warp - 2) >> 2;  // two warps per quarter split the columns
+        const int q = warp & 3;                    // TMEM lane quarter this warp may read
+        const int colq = warp < 7 ? 0 : 1;  // two warps per quarter split the columns
         const int row = q * 32 + lane;
         const int n = feat0 + row;
         const bool live = ok && !*abort_flag;
         float bias = 0.0f;
         if (!kF32Out && live && p.bias != nullptr && n < p.N && gridDim.z == 1)
             bias = __half2float(p.bias[n]);
-        for (int c0 = 16 * colhalf; c0 < p.nt; c0 += 32) {
+        for (int c0 = 16 * colq; c0 < p.nt; c0 += 32) {
             uint32_t r[16];
+            __syncwarp();   // the stores of the previous round diverge
             tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, r);
             tmem_wait_ld();
             if (!live || n >= p.N) continue;
@@ -300,12 +489,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        }
     }
-
+done:
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, ncols);
+    // No CTA leaves while a peer may still multicast into it or arrive on its
+    // barriers.
+    cluster_sync_all();
+    if (*abort_flag && threadIdx.x == 0) {
+        // after an expired wait, give any stray multicast copy time to land
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) {
+        }
+    }
 }
 
 // Fixed-order sum of the K-split partials, then the epilogue.
@@ -375,30 +574,69 @@ fg_status make_tmap(CUtensorMap* tm, const void* ptr, CUtensorMapDataType dt, in
     return FG_OK;
 }
 
-int stages_for(int nt, bool dq) {
-    const int per = static_cast<int>(kABytes + nt * 128 + (dq ? kCBytes : 0));
-    int s = (kSmemLimit - 1024 - 8 * (3 * kMaxStages + 1) - 16) / per;
-    if (s > kMaxStages) s = kMaxStages;
-    return s;
+struct Rings {
+    int ns, sc;
+    size_t smem;
+};
+
+Rings rings_for(int nt, bool dq) {
+    // every barrier must fit the space reserved for kMaxBars
+    static_assert(2 * (kCStages + kMaxStages) + 1 <= kMaxBars, "barrier space");
+    Rings r{};
+    const size_t per = kABytes + static_cast<size_t>(nt) * 128;
+    // dequant mode: as many codes boxes as leave kMinStagesDq stages (the
+    // parity rule), preferring 3 boxes in flight
+    for (int sc = dq ? kCStages : 0; sc >= 0; --sc) {
+        const size_t fixed = 1024 + static_cast<size_t>(sc) * kCBytes + 8 * kMaxBars + 16;
+        int ns = static_cast<int>((kSmemLimit - fixed) / per);
+        if (ns > kMaxStages) ns = kMaxStages;
+        r.sc = sc;
+        r.ns = ns;
+        r.smem = fixed + static_cast<size_t>(ns) * per;
+        if (!dq || ns >= kMinStagesDq) break;
+    }
+    return r;
 }
 
-size_t smem_for(int nt, bool dq, int stages) {
-    return 1024 + static_cast<size_t>(stages) * (kABytes + nt * 128 + (dq ? kCBytes : 0)) +
-           8 * (3 * stages + 1) + 16;
+// CTAs per cluster sharing one activation tile: the largest of 4, 2, 1 that
+// divides the feature tiles and leaves slices of whole 8-row swizzle atoms.
+int cluster_for(int feat_tiles, int nt) {
+    for (int c = 4; c > 1; c >>= 1)
+        if (feat_tiles % c == 0 && nt % c == 0 && (nt / c) % 8 == 0) return c;
+    return 1;
 }
 
 template <bool kDequant, bool kF32Out>
-fg_status run_gemm(const CUtensorMap& tmX, const CUtensorMap& tmW, GemmParams& p,
-                   const fg::GemmPlan& plan, cudaStream_t st) {
-    p.stages = stages_for(plan.nt, kDequant);
-    const size_t smem = smem_for(plan.nt, kDequant, p.stages);
-    auto kern = gemm_tc_kernel<kDequant, kF32Out>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return fg::cuda_error(e, "gemm smem attribute");
-    dim3 grid(plan.feat_tiles * plan.tok_tiles, 1, plan.splits);
+fg_status run_gemm(const void* X, const CUtensorMap& tmW, GemmParams& p, const fg::GemmPlan& plan,
+                   cudaStream_t st) {
+    const Rings rg = rings_for(plan.nt, kDequant);
+    if (rg.ns < (kDequant ? kMinStagesDq : 2) || (kDequant && rg.sc < 1))
+        return fg::set_error(FG_ERR_UNSUPPORTED, "gemm: tile of %d rows does not fit", plan.nt);
+    p.ns = rg.ns;
+    p.sc = rg.sc;
+    p.cluster = cluster_for(plan.feat_tiles, plan.nt);
     p.feat_tiles = plan.feat_tiles;
     p.tok_tiles = plan.tok_tiles;
+    CUtensorMap tmX;
+    fg_status s = make_tmap(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.K, p.M, kChunk,
+                            plan.nt / p.cluster, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s != FG_OK) return s;
+    auto kern = gemm_tc_kernel<kDequant, kF32Out>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(rg.smem));
+    if (e != cudaSuccess) return fg::cuda_error(e, "gemm smem attribute");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.feat_tiles * plan.tok_tiles, 1, plan.splits);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = rg.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     const double M = p.M, N = p.N, K = p.K;
     // algorithmic traffic: the weight once (4-bit codes + fp32 (min, scale) per
     // 64, or fp16), X once, Y once (+ residual, or fp32 partials / logits)
@@ -409,7 +647,8 @@ fg_status run_gemm(const CUtensorMap& tmX, const CUtensorMap& tmW, GemmParams& p
     const int cls = !kDequant ? FG_TRACE_OTHER
                               : (p.M > 256 ? FG_TRACE_GEMM_PREFILL : FG_TRACE_GEMM_DECODE);
     fg::TraceScope ts(cls, st, 2.0 * M * N * K, wbytes + M * K * 2.0 + ybytes);
-    kern<<<grid, kThreads, smem, st>>>(tmX, tmW, p);
+    e = cudaLaunchKernelEx(&cfg, kern, tmX, tmW, p);
+    if (e != cudaSuccess) return fg::cuda_error(e, "gemm launch");
     return fg::cuda_error(cudaGetLastError(), "gemm launch");
 }
 
@@ -439,10 +678,12 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K) {
         if (s < 1) s = 1;
         pl.splits = s;
     }
+    pl.kc_per_split = static_cast<int>(kchunks);
     if (pl.splits > 1) {
-        // equalise the chunk ranges; drop splits that would be empty
-        const int64_t per = cdiv(kchunks, pl.splits);
+        // equal ranges of whole codes boxes (4 K chunks); drop empty splits
+        const int64_t per = cdiv(cdiv(kchunks, pl.splits), kCodeSpan) * kCodeSpan;
         pl.splits = static_cast<int>(cdiv(kchunks, per));
+        pl.kc_per_split = static_cast<int>(per);
     }
     pl.ws_bytes = pl.splits > 1 ? static_cast<size_t>(pl.splits) * M * N * sizeof(float) : 0;
     return pl;
@@ -457,12 +698,10 @@ fg_status launch_gemm_g4(const __half* X, int64_t M, const fg_q4* W, const __hal
     if (pl.ws_bytes > 0 && (ws == nullptr || ws_bytes < pl.ws_bytes))
         return set_error(FG_ERR_WORKSPACE, "dequant_gemm: workspace %zu < %zu bytes", ws_bytes,
                          pl.ws_bytes);
-    CUtensorMap tmX, tmC;
-    fg_status s = make_tmap(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, K, M, kChunk, pl.nt,
-                            CU_TENSOR_MAP_SWIZZLE_128B);
-    if (s != FG_OK) return s;
-    s = make_tmap(&tmC, W->codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N, kChunk / 2, kTileF,
-                  CU_TENSOR_MAP_SWIZZLE_NONE);
+    // codes: one box = 128 rows x 128 bytes (4 K chunks), 128-byte swizzle
+    CUtensorMap tmC;
+    fg_status s = make_tmap(&tmC, W->codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N,
+                            kCodeSpan * kChunk / 2, kTileF, CU_TENSOR_MAP_SWIZZLE_128B);
     if (s != FG_OK) return s;
     GemmParams p{};
     p.meta = reinterpret_cast<const float2*>(W->meta);
@@ -475,12 +714,12 @@ fg_status launch_gemm_g4(const __half* X, int64_t M, const fg_q4* W, const __hal
     p.K = static_cast<int>(K);
     p.nt = pl.nt;
     p.kchunks = static_cast<int>(K / kChunk);
-    p.kc_per_split = static_cast<int>(cdiv(p.kchunks, pl.splits));
+    p.kc_per_split = pl.kc_per_split;
     p.act = act;
     p.status = device_status_ptr();
     p.wait_ns = wait_limit_ns();
     p.drop_arrive = take_drop_arrive();
-    s = run_gemm<true, false>(tmX, tmC, p, pl, st);
+    s = run_gemm<true, false>(X, tmC, p, pl, st);
     if (s != FG_OK || pl.splits == 1) return s;
     const int64_t nv = M * N / 4;
     int64_t blocks = cdiv(nv, 256);
@@ -496,12 +735,9 @@ fg_status launch_gemm_f16_f32out(const __half* X, int64_t M, const __half* W, in
     if (M == 0) return FG_OK;
     GemmPlan pl = plan_gemm(M, N, K);
     pl.splits = 1;
-    CUtensorMap tmX, tmW;
-    fg_status s = make_tmap(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, K, M, kChunk, pl.nt,
+    CUtensorMap tmW;
+    fg_status s = make_tmap(&tmW, W, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, K, N, kChunk, kTileF,
                             CU_TENSOR_MAP_SWIZZLE_128B);
-    if (s != FG_OK) return s;
-    s = make_tmap(&tmW, W, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, K, N, kChunk, kTileF,
-                  CU_TENSOR_MAP_SWIZZLE_128B);
     if (s != FG_OK) return s;
     GemmParams p{};
     p.Yf = Y;
@@ -513,7 +749,7 @@ fg_status launch_gemm_f16_f32out(const __half* X, int64_t M, const __half* W, in
     p.kc_per_split = p.kchunks;
     p.status = device_status_ptr();
     p.wait_ns = wait_limit_ns();
-    return run_gemm<false, true>(tmX, tmW, p, pl, st);
+    return run_gemm<false, true>(X, tmW, p, pl, st);
 }
 
 }  // namespace fg
