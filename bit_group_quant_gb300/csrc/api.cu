@@ -99,7 +99,7 @@ LayerWs layer_ws_layout(const fg_layer* w, int64_t rows, int64_t rows_per_launch
     size_t g = 0;
     const int64_t NK[4][2] = {{3 * h1, h1}, {h1, h1}, {h2, h1}, {h1, h2}};
     for (auto& nk : NK) {
-        const fg::GemmPlan pl = fg::plan_gemm(rows_per_launch, nk[0], nk[1]);
+        const fg::GemmPlan pl = fg::plan_gemm(rows_per_launch, nk[0], nk[1], rows);
         if (pl.ws_bytes > g) g = pl.ws_bytes;
     }
     L.gemm_bytes = g;
@@ -521,7 +521,7 @@ fg_status fg_layer_step(const fg_layer* w, const fg_kv4* cache, const fg_f16* x_
     } while (0)
         FG_RUN(fg::launch_layernorm(xin, nr, h1, h1, H(w->ln1_g), H(w->ln1_b), w->ln_eps, a, st));
         FG_RUN(fg::launch_gemm_g4(a, nr, &w->qkv, H(w->b_qkv), nullptr, FG_ACT_NONE, qkv, L.gemm,
-                                  L.gemm_bytes, st));
+                                  L.gemm_bytes, st, rows));
         if (phase == FG_PHASE_PREFILL) {
             FG_RUN(fg::launch_prefill_attn(qkv, nb, T, w->H, d, attn, st));
             FG_RUN(fg::launch_kv_store(qkv, 3 * h1, nb, T, w->H, d, &c, 0, st));
@@ -529,12 +529,12 @@ fg_status fg_layer_step(const fg_layer* w, const fg_kv4* cache, const fg_f16* x_
             FG_RUN(fg::launch_decode_attn(qkv, 3 * h1, &c, pos, 1, attn, st));
         }
         FG_RUN(fg::launch_gemm_g4(attn, nr, &w->out, H(w->b_out), xin, FG_ACT_NONE, hh, L.gemm,
-                                  L.gemm_bytes, st));
+                                  L.gemm_bytes, st, rows));
         FG_RUN(fg::launch_layernorm(hh, nr, h1, h1, H(w->ln2_g), H(w->ln2_b), w->ln_eps, a, st));
         FG_RUN(fg::launch_gemm_g4(a, nr, &w->fc1, H(w->b_fc1), nullptr, FG_ACT_RELU, u, L.gemm,
-                                  L.gemm_bytes, st));
+                                  L.gemm_bytes, st, rows));
         FG_RUN(fg::launch_gemm_g4(u, nr, &w->fc2, H(w->b_fc2), hh, FG_ACT_NONE, xout, L.gemm,
-                                  L.gemm_bytes, st));
+                                  L.gemm_bytes, st, rows));
 #undef FG_RUN
     }
     return FG_OK;

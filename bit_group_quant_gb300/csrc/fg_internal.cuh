@@ -67,14 +67,18 @@ struct GemmPlan {
     int nt;          // activation rows per tile (MMA N), multiple of 16, <= 256
     int tok_tiles;
     int feat_tiles;  // ceil(N / 128)
-    int splits;      // K splits (grid.z); > 1 only when tok_tiles == 1
+    int splits;      // K splits (grid.z); > 1 only when plan_rows fit one token tile
     int kc_per_split;  // K chunks (of 64) per split, a multiple of 4
     size_t ws_bytes; // fp32 partial sums when splits > 1
 };
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K);
+// The summation order of every output -- hence its value -- depends on (N, K)
+// and on whether plan_rows fits one 256-row token tile, never on M itself:
+// launches that must give identical rows (the batches of one block and the
+// whole block) pass the same plan_rows.  plan_rows < M means plan_rows = M.
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int64_t plan_rows = 0);
 fg_status launch_gemm_g4(const __half* X, int64_t M, const fg_q4* W, const __half* bias,
                          const __half* residual, int act, __half* Y, void* ws, size_t ws_bytes,
-                         cudaStream_t st);
+                         cudaStream_t st, int64_t plan_rows = 0);
 fg_status launch_gemm_f16_f32out(const __half* X, int64_t M, const __half* W, int64_t N,
                                  int64_t K, float* Y, cudaStream_t st);
 

@@ -17,16 +17,18 @@
 // slice to the whole cluster, so the activations cross L2 once per cluster
 // instead of once per CTA.
 //
-// Warp roles (352 threads): warp 0 = TMA producer of the weight side (packed
-// codes, 4 K-chunks per 128-byte-swizzled box, or fp16 A tiles); warp 2 =
-// TMA producer of this CTA's activation slices; warp 1 = TMEM allocator and
-// the single MMA-issuing thread; warps 3-10 = dequantisers in four groups of
-// two, group g owning K chunks g, g+4, ... (two weight rows per thread: 32
-// code bytes + (min, scale) -> 64 fp16 each, written in the 128-byte-swizzled
-// K-major layout the MMA descriptor reads), then the epilogue (tcgen05.ld of
-// the accumulator, bias / ReLU / residual, fp16 store) -- or fp32 partial sums
-// when K is split.  Tiles are visited in groups of 16 feature tiles x all
-// token tiles, and each group of 4 feature tiles starts its K walk at its own
+// Warp roles (416 threads, 13 warps): warp 0 = TMA producer of the weight
+// side (packed codes, 4 K-chunks per 128-byte-swizzled box, or fp16 A tiles);
+// warp 2 = TMA producer of this CTA's activation slices; warp 1 = TMEM
+// allocator and the single MMA-issuing thread, alone on its sub-partition
+// during the mainloop (warps 5 and 9 idle until the epilogue); warps 3, 4, 6,
+// 7, 8, 10, 11, 12 = dequantisers in four groups of two, group g owning K
+// chunks g, g+4, ... (two weight rows per thread: 32 code bytes + (min,
+// scale) -> 64 fp16 each, written in the 128-byte-swizzled K-major layout the
+// MMA descriptor reads).  Warps 3-10 then run the epilogue (tcgen05.ld of the
+// accumulator, bias / ReLU / residual, fp16 store -- or fp32 partial sums when
+// K is split).  Tiles are visited in groups of 16 feature tiles x all token
+// tiles, and each group of 4 feature tiles starts its K walk at its own
 // offset, so L2 sees neither re-reads nor hot spots.
 //
 // Every mbarrier wait is bounded; a wait that expires flags the CTA to stop,
@@ -86,31 +88,29 @@ struct GemmParams {
     int drop_arrive;
 };
 
-// 8 codes (one 32-bit word, element 0 in the lowest nibble) -> 8 fp16
-// m + c*s as four half2 words in element order.  (1024 + c) is exact in fp16
-// when the code is OR-ed into the mantissa of 1024; subtracting 1024 leaves c
-// exactly, and one fused half2 multiply-add applies scale and min.
-__device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2, __half2 m2) {
-    const uint32_t kMagic = 0x64006400u;  // half2(1024, 1024)
-    const __half2 k1024 = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
-    uint32_t t[4];
-    t[0] = (w & 0x000F000Fu) | kMagic;          // (c0, c4)
-    t[1] = ((w >> 4) & 0x000F000Fu) | kMagic;   // (c1, c5)
-    t[2] = ((w >> 8) & 0x000F000Fu) | kMagic;   // (c2, c6)
-    t[3] = ((w >> 12) & 0x000F000Fu) | kMagic;  // (c3, c7)
-    uint32_t y[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        __half2 c = __hsub2(*reinterpret_cast<__half2*>(&t[i]), k1024);
-        __half2 v = __hfma2(c, s2, m2);
-        y[i] = *reinterpret_cast<uint32_t*>(&v);
-    }
-    uint4 r;
-    r.x = __byte_perm(y[0], y[1], 0x5410);  // (c0, c1)
-    r.y = __byte_perm(y[2], y[3], 0x5410);  // (c2, c3)
-    r.z = __byte_perm(y[0], y[1], 0x7632);  // (c4, c5)
-    r.w = __byte_perm(y[2], y[3], 0x7632);  // (c6, c7)
-    return r;
+// 8 codes (one 32-bit word, element 0 in the lowest nibble) -> the 8 fp16
+// values fp16(fma(c, s, m)): one fp32 fused multiply-add, then round to
+// nearest even -- the dequantisation of the definition, bit for bit.
+//
+// A code is masked into an fp16 word as the subnormal c * 2^-24 (nibbles 1
+// and 3 of each byte pair are taken in place, as 16c * 2^-24), converted to
+// fp32 exactly, and multiplied by S = s * 2^24 (S16 = s * 2^20): the product
+// is exactly c * s, so the fma rounds c*s + m once, as the definition does.
+// (Scaling s by a power of two is exact: fp16 inputs bound s below 2^14.)
+__device__ __forceinline__ uint4 dequant8(uint32_t w, float S, float S16, float m) {
+    const uint32_t w8 = w >> 8;
+    const uint32_t t0 = w & 0x000F000Fu, t1 = w & 0x00F000F0u;     // (c0, c4), (16c1, 16c5)
+    const uint32_t t2 = w8 & 0x000F000Fu, t3 = w8 & 0x00F000F0u;   // (c2, c6), (16c3, 16c7)
+    const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&t0));
+    const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&t1));
+    const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&t2));
+    const float2 a3 = __half22float2(*reinterpret_cast<const __half2*>(&t3));
+    __half2 h[4];
+    h[0] = __floats2half2_rn(__fmaf_rn(a0.x, S, m), __fmaf_rn(a1.x, S16, m));   // (e0, e1)
+    h[1] = __floats2half2_rn(__fmaf_rn(a2.x, S, m), __fmaf_rn(a3.x, S16, m));   // (e2, e3)
+    h[2] = __floats2half2_rn(__fmaf_rn(a0.y, S, m), __fmaf_rn(a1.y, S16, m));   // (e4, e5)
+    h[3] = __floats2half2_rn(__fmaf_rn(a2.y, S, m), __fmaf_rn(a3.y, S16, m));   // (e6, e7)
+    return *reinterpret_cast<uint4*>(h);
 }
 
 // Dequantiser index 0..7 of a warp (-1 for other warps).  Sub-partition 1
@@ -417,15 +417,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint4 wb0 = *reinterpret_cast<const uint4*>(c0p + u1);
                     const uint4 wa1 = *reinterpret_cast<const uint4*>(c1p + u0);
                     const uint4 wb1 = *reinterpret_cast<const uint4*>(c1p + u1);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(sm.c_empty(sc));
+                    // The codes box is released only after the proxy fence
+                    // below: the next box is written into the slot by TMA (the
+                    // async proxy), and an mbarrier release alone does not
+                    // order these generic reads before that write -- with an
+                    // arrive right here, runs with thousands of boxes per CTA
+                    // dequantised codes the TMA had already replaced.
                     if (!__all_sync(0xffffffffu, mbar_wait(sm.empty(sa), pa ^ 1u, abort_flag, lim))) {
                         fail();
                         stop = true;
                         break;
                     }
-                    const __half2 s20 = __float2half2_rn(mm0.y), m20 = __float2half2_rn(mm0.x);
-                    const __half2 s21 = __float2half2_rn(mm1.y), m21 = __float2half2_rn(mm1.x);
+                    const float S0 = mm0.y * 16777216.0f, S160 = mm0.y * 1048576.0f;
+                    const float S1 = mm1.y * 16777216.0f, S161 = mm1.y * 1048576.0f;
                     const uint32_t w0[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wb0.x, wb0.y, wb0.z, wb0.w};
                     const uint32_t w1[8] = {wa1.x, wa1.y, wa1.z, wa1.w, wb1.x, wb1.y, wb1.z, wb1.w};
                     uint8_t* a0p = gen + sm.a(sa) + r0 * 128;
@@ -433,12 +437,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         const uint32_t off = (c ^ (r0 & 7)) << 4;
-                        *reinterpret_cast<uint4*>(a0p + off) = dequant8(w0[c], s20, m20);
-                        *reinterpret_cast<uint4*>(a1p + off) = dequant8(w1[c], s21, m21);
+                        *reinterpret_cast<uint4*>(a0p + off) = dequant8(w0[c], S0, S160, mm0.x);
+                        *reinterpret_cast<uint4*>(a1p + off) = dequant8(w1[c], S1, S161, mm1.x);
                     }
+                    // one fence orders this warp's generic smem accesses before
+                    // the async proxy: the A stores before the MMA reads them,
+                    // and the codes reads before TMA overwrites the box
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(sm.full(sa));
+                    if (lane == 0) {
+                        mbar_arrive(sm.full(sa));
+                        mbar_arrive(sm.c_empty(sc));
+                    }
                     // next chunk of this group: codes box +1, stage +4 (mod NS)
                     if (++sc == sm.sc) { sc = 0; pc ^= 1u; }
                     sa += kDeqGroups;
@@ -660,8 +670,9 @@ namespace fg {
 // tiles, and the K split only on (N, K) -- and is used only when all rows fit
 // one tile -- so every row's result is independent of M and of the other rows
 // (the row-by-row and zig-zag block orders must agree bit for bit).
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K) {
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int64_t plan_rows) {
     GemmPlan pl{};
+    if (plan_rows < M) plan_rows = M;
     pl.tok_tiles = static_cast<int>(cdiv(M, 256));
     if (pl.tok_tiles < 1) pl.tok_tiles = 1;
     int64_t rows = cdiv(M, pl.tok_tiles);
@@ -670,7 +681,7 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K) {
     pl.feat_tiles = static_cast<int>(cdiv(N, kTileF));
     pl.splits = 1;
     const int64_t kchunks = K / kChunk;
-    if (pl.tok_tiles == 1) {
+    if (plan_rows <= 256) {   // one token tile: split K to fill the SMs
         const int sms = num_sms();
         int s = sms / pl.feat_tiles;
         if (s > 8) s = 8;
@@ -691,10 +702,10 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K) {
 
 fg_status launch_gemm_g4(const __half* X, int64_t M, const fg_q4* W, const __half* bias,
                          const __half* residual, int act, __half* Y, void* ws, size_t ws_bytes,
-                         cudaStream_t st) {
+                         cudaStream_t st, int64_t plan_rows) {
     if (M == 0) return FG_OK;
     const int64_t N = W->rows, K = W->cols;
-    const GemmPlan pl = plan_gemm(M, N, K);
+    const GemmPlan pl = plan_gemm(M, N, K, plan_rows);
     if (pl.ws_bytes > 0 && (ws == nullptr || ws_bytes < pl.ws_bytes))
         return set_error(FG_ERR_WORKSPACE, "dequant_gemm: workspace %zu < %zu bytes", ws_bytes,
                          pl.ws_bytes);

@@ -89,7 +89,9 @@ typedef struct fg_kv4 {
  * order FG_ORDER_BATCHES / FG_ORDER_BATCHES_REV: the k GPU batches run as k
  *   launches per projection in ascending / descending batch order (the
  *   zig-zag schedule alternates the two at each token step).
- * Every order gives bit-identical results. */
+ * Every order gives bit-identical results: every launch of a block plans
+ * its K split from the block's row count (bls * T), so the batches and the
+ * whole block sum each output in the same order. */
 enum { FG_ORDER_BLOCK = 0, FG_ORDER_BATCHES = 1, FG_ORDER_BATCHES_REV = 2 };
 typedef struct fg_policy {
     int32_t gbs;
@@ -154,8 +156,13 @@ fg_status fg_dequant_g4(const fg_q4* in, fg_f16* x, fg_stream stream);
  * Y: [M][N] fp16.  M >= 0 (M == 0 launches nothing); N % 16 == 0.
  * workspace: device scratch of at least
  * fg_dequant_gemm_workspace_bytes(M, N, K) bytes (NULL allowed when that is
- * 0), 256-byte aligned.  The result of each row does not depend on M or on
- * the other rows. */
+ * 0), 256-byte aligned.
+ * Each output is fp32-accumulated fp16(x) * fp16(w^) products with
+ * w^ = fp16(fma(q, scale, min)) exactly as fg_dequant_g4 gives it.  The
+ * result of a row never depends on the other rows; it depends on M only
+ * through one switch -- whether M <= 256 (then K may be split across CTAs
+ * and summed in a fixed order) -- so launches of 1..256 rows agree bit for
+ * bit, as do launches of more than 256 rows. */
 size_t fg_dequant_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 fg_status fg_dequant_gemm_g4(const fg_f16* X, int64_t M, const fg_q4* W,
                              const fg_f16* bias, const fg_f16* residual,

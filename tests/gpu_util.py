@@ -21,21 +21,21 @@ def unpack_codes(codes):
 
 
 def gemm_bound(x, codes, meta, extra_abs=0.0):
-    """Per-element bound |Y_gpu - Y_oracle| for the 4-bit linear layer:
-    the GPU dequantises with one fused fp16 multiply-add on fp16-rounded
-    (min, scale), the oracle with one fp32 fused multiply-add rounded to fp16;
-    each weight then differs by at most 2^-10 (|m| + q*s + |w^|).  Both
-    accumulate fp16 x fp16 products in fp32 (orders differ: K * 2^-23 of the
-    absolute dot product), then one fp16 rounding of Y (1 ulp between two
-    roundings)."""
+    """Per-element bound |Y_gpu - Y_oracle| for the 4-bit linear layer.
+
+    Both sides multiply by the same dequantised weights w^ = fp16(fma(q, s,
+    m)) (the GPU's fused dequantisation is bit-exact with the oracle's), and
+    fp16 x fp16 products are exact in fp32, so only the fp32 summation orders
+    differ: at most K * 2^-23 of the absolute dot product sum |x| |w^| between
+    the two (each side <= K/2 * 2^-23).  Callers add one fp16 ulp of Y for the
+    final rounding."""
     q = unpack_codes(codes).astype(np.float64)
     N, K = q.shape
-    m = np.repeat(np.abs(meta[..., 0].astype(np.float64)), 64, axis=1)
-    s = np.repeat(np.abs(meta[..., 1].astype(np.float64)), 64, axis=1)
-    wmag = m + q * s
+    m = np.repeat(meta[..., 0].astype(np.float64), 64, axis=1)
+    s = np.repeat(meta[..., 1].astype(np.float64), 64, axis=1)
+    wmag = np.abs(m + q * s) * (1.0 + 2.0 ** -10)   # >= |w^| (one fp16 rounding)
     xa = np.abs(x.astype(np.float64))
-    dot_abs = xa @ wmag.T
-    return 2.0 ** -9 * dot_abs + K * 2.0 ** -23 * dot_abs + extra_abs
+    return K * 2.0 ** -23 * (xa @ wmag.T) + extra_abs
 
 
 def ulp16(y):

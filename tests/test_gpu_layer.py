@@ -71,6 +71,31 @@ def test_block_orders_bitwise_identical_on_gpu():
         assert torch.equal(x, y) and torch.equal(x, z)
 
 
+def test_block_orders_identical_when_block_exceeds_one_token_tile():
+    """gbs 64 x k 5 = 320 sequences, h1 256 / 4 heads / h2 1024: a decode
+    block of 320 rows takes two token tiles, while each 64-row batch alone
+    would fit one (where the K = 1024 projection splits K across CTAs).  The
+    batches plan their split from the block, so all orders still agree bit
+    for bit."""
+    h1, H, h2, gbs, k, s = 256, 4, 1024, 64, 5, 8
+    gl, _, g = _layer(h1, H, h2, 11)
+    assert fg.fg_dequant_gemm_workspace_bytes(gbs, h1, h2) > 0      # split alone
+    assert fg.fg_dequant_gemm_workspace_bytes(gbs * k, h1, h2) == 0
+    x = synth.normal_f16((gbs * k * s, h1), 1.0, g).to(DEV)
+    xs = [synth.normal_f16((gbs * k, h1), 1.0, g).to(DEV) for _ in range(2)]
+    outs = []
+    for order in (lambda t: fg.FG_ORDER_BLOCK, lambda t: fg.FG_ORDER_BATCHES,
+                  lambda t: fg.FG_ORDER_BATCHES if t % 2 == 0 else fg.FG_ORDER_BATCHES_REV):
+        stack = LayerStack([gl], gbs, k, s + 3, DEV)
+        ys = [stack.run(x, fg.FG_PHASE_PREFILL, s, 0, order(0)).clone()]
+        for t in (1, 2):
+            ys.append(stack.run(xs[t - 1], fg.FG_PHASE_DECODE, 1, s + t - 1, order(t)).clone())
+        outs.append(ys)
+    fg.fg_check()
+    for a, b, c in zip(*outs):
+        assert torch.equal(a, b) and torch.equal(a, c)
+
+
 def test_small_model_logits_match_oracle():
     """2 layers of h1 512 / 8 heads / h2 1024, vocab 1000, gbs 2 x k 2,
     prompt 24, 3 decode steps: teacher-forced logits every step within
