@@ -326,6 +326,322 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
     }
 }
 
+// Decode attention for d = 128 with the cache streamed through shared memory.
+// Same arithmetic as decode_attn_kernel; the data path differs: for one
+// (head, sequence) the L cached rows of K codes, K (min, scale), V codes and
+// V (min, scale) are four contiguous regions, fetched in chunks of kCK rows by
+// 1-D bulk asynchronous copies (the async proxy) into a ring of kNB chunk
+// buffers -- K chunks first, then V chunks, so V streams in while the K pass
+// computes.  Thread 0 refills a buffer after the block barrier that ends its
+// use; every wait on a chunk is bounded.
+// 128-key chunks, 2 buffers (23 KB per block) and <= 64 registers give 8
+// blocks per SM: with the 2 block barriers per chunk, many resident blocks
+// keep more bytes in flight than deeper rings would (measured on GB300:
+// 4.1-4.7 TB/s at contexts 513-2049, against 3.5-4.2 with 4 x 128 keys).
+constexpr int kCK = 128;           // keys per staged chunk
+constexpr int kNB = 2;             // chunk buffers
+constexpr int kMinBlocks = 8;      // resident blocks per SM (register cap)
+constexpr int kCKMax = kCK + 16;   // the last chunk absorbs a remainder of up to 16 keys
+constexpr int kRB128 = 64;         // code bytes per row (d = 128)
+constexpr int kMB128 = 16;         // (min, scale) bytes per row (2 groups)
+constexpr int kChunkBytes = kCKMax * (kRB128 + kMB128);   // codes, then meta
+
+__global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_kernel(
+    const __half* __restrict__ qkv, int64_t ld, int32_t H, int32_t cap, int32_t pos,
+    int32_t fuse_append, uint8_t* k_codes, uint8_t* v_codes, float* k_meta, float* v_meta,
+    __half* __restrict__ out, int* status, unsigned long long wait_ns) {
+    constexpr int D = 128, G = 2, RB = kRB128, WPT = D / 32, NX = 2 * WPT;
+    constexpr int NWARP = kDecThreads / 32;
+    extern __shared__ __align__(128) uint8_t dyn[];
+    __shared__ __align__(8) uint64_t full_bar[kNB];
+    __shared__ float qsum[G];
+    __shared__ float red[NWARP];
+    __shared__ float part[NWARP][D];
+    __shared__ float part_s[NWARP][2][2];
+
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int L = pos + 1;
+    // chunks of kCK keys; a remainder of <= 16 keys joins the last full chunk
+    int nK = (L + kCK - 1) / kCK;
+    if (nK > 1 && L - (nK - 1) * kCK <= 16) --nK;
+    const int nseq = 2 * nK;
+    auto chunk_n = [&](int c) { return c == nK - 1 ? L - c * kCK : kCK; };
+    const int64_t h1 = static_cast<int64_t>(H) * D;
+    const int64_t row0 = (static_cast<int64_t>(b) * H + h) * cap;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const uint32_t ring = smem_u32(dyn);
+    float* sc = reinterpret_cast<float*>(dyn + kNB * kChunkBytes);
+
+    if (fuse_append && warp == 0) {
+        const int grp = lane >> 3, lane8 = lane & 7;
+        const bool valid = grp < 2 * G;
+        const int is_v = grp / G, gi = grp % G;
+        float v[8];
+        if (valid) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(
+                qkv + b * ld + (1 + is_v) * h1 + static_cast<int64_t>(h) * D + gi * 64 + lane8 * 8);
+            const __half2* hh = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __half22float2(hh[i]);
+                v[2 * i] = f.x;
+                v[2 * i + 1] = f.y;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+        }
+        float mn, scale;
+        const uint32_t packed = quantize8(v, mn, scale);
+        if (valid) {
+            const int64_t row = row0 + pos;
+            uint8_t* cdst = (is_v ? v_codes : k_codes) + row * RB + gi * 32;
+            reinterpret_cast<uint32_t*>(cdst)[lane8] = packed;
+            if (lane8 == 0) {
+                float* mdst = (is_v ? v_meta : k_meta) + (row * G + gi) * 2;
+                *reinterpret_cast<float2*>(mdst) = make_float2(mn, scale);
+            }
+        }
+        // the appended row is read back below by bulk copies (async proxy)
+        fence_proxy_async_global();
+    }
+    const __half* qrow = qkv + b * ld + static_cast<int64_t>(h) * D;
+    if (warp == 1) {   // per-group sums of q (fp32)
+        float s0 = 0.0f, s1 = 0.0f;
+        for (int i = lane; i < D; i += 32) {
+            const float qv = __half2float(qrow[i]);
+            if (i < 64) s0 += qv; else s1 += qv;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+            s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        }
+        if (lane == 0) {
+            qsum[0] = s0;
+            qsum[1] = s1;
+        }
+    }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNB; ++i) mbar_init(smem_u32(&full_bar[i]), 1);
+        fence_mbar_init();
+    }
+    // q as the B operand of the pass-1 MMAs (see decode_attn_kernel)
+    uint32_t qb[NX][2];
+    {
+        const int my_grp = (WPT * t * 8) / 64;
+        const bool use = g < G && g == my_grp;
+#pragma unroll
+        for (int x = 0; x < NX; ++x) {
+            const int base = 8 * (WPT * t + (x >> 1)) + 2 * (x & 1);
+            const float q0 = use ? __half2float(qrow[base]) : 0.0f;
+            const float q4 = use ? __half2float(qrow[base + 4]) : 0.0f;
+            const float q1 = use ? __half2float(qrow[base + 1]) : 0.0f;
+            const float q5 = use ? __half2float(qrow[base + 5]) : 0.0f;
+            qb[x][0] = pack_h2(q0, q4);
+            qb[x][1] = pack_h2(q1, q5);
+        }
+    }
+    __syncthreads();
+
+    // chunk seq: K chunks 0..nK-1, then V chunks; buffer seq % kNB, phase seq / kNB
+    auto issue = [&](int seq) {
+        const bool is_v = seq >= nK;
+        const int c = is_v ? seq - nK : seq;
+        const int r0 = c * kCK, n = chunk_n(c);
+        const int slot = seq % kNB;
+        const uint32_t dst = ring + slot * kChunkBytes;
+        const uint32_t bar = smem_u32(&full_bar[slot]);
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * (RB + kMB128)));
+        bulk_load(dst, (is_v ? v_codes : k_codes) + (row0 + r0) * RB, n * RB, bar);
+        bulk_load(dst + kCKMax * RB, (is_v ? v_meta : k_meta) + (row0 + r0) * G * 2, n * kMB128, bar);
+    };
+    int issued_hi = -1;   // thread 0: highest chunk seq issued so far
+    if (threadIdx.x == 0)
+        for (int i = 0; i < kNB && i < nseq; ++i) issue(issued_hi = i);
+    // bounded wait for chunk seq, made uniform over the block; false = give up
+    auto wait_chunk = [&](int seq) {
+        const bool ok = mbar_wait(smem_u32(&full_bar[seq % kNB]), (seq / kNB) & 1, nullptr, wait_ns);
+        return __syncthreads_and(ok ? 1 : 0) != 0;
+    };
+    bool failed = false;
+
+    const float attn_scale = __fdiv_rn(1.0f, __fsqrt_rn(static_cast<float>(D)));
+    const float Q0 = qsum[0], Q1 = qsum[1];
+
+    // ---------------- pass 1: scores
+    float lmax = -CUDART_INF_F;
+    for (int c = 0; c < nK && !failed; ++c) {
+        if (!wait_chunk(c)) {
+            failed = true;
+            break;
+        }
+        const uint8_t* buf = dyn + (c % kNB) * kChunkBytes;
+        const int r0 = c * kCK, n = chunk_n(c);
+        const int ntile = (n + 15) >> 4;
+        for (int kt = warp; kt < ntile; kt += NWARP) {
+            const int ja = min(kt * 16 + g, n - 1), jb = min(kt * 16 + g + 8, n - 1);
+            const uint4 va = *reinterpret_cast<const uint4*>(buf + ja * RB + t * 16);
+            const uint4 vb = *reinterpret_cast<const uint4*>(buf + jb * RB + t * 16);
+            const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
+            const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            __syncwarp();
+#pragma unroll
+            for (int x = 0; x < NX; ++x) {
+                const int e = 2 * (x & 1);
+                mma16816(acc, nib_pair(wa[x >> 1], e), nib_pair(wb[x >> 1], e),
+                         nib_pair(wa[x >> 1], e + 1), nib_pair(wb[x >> 1], e + 1), qb[x][0], qb[x][1]);
+            }
+            if (t == 0) {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int jl = kt * 16 + g + 8 * half;
+                    if (jl < n) {
+                        const float4 m = *reinterpret_cast<const float4*>(buf + kCKMax * RB + jl * kMB128);
+                        const float dot = m.x * Q0 + 16.0f * m.y * (acc[2 * half] - Q0) +
+                                          m.z * Q1 + 16.0f * m.w * (acc[2 * half + 1] - Q1);
+                        const float s = dot * attn_scale;
+                        sc[r0 + jl] = s;
+                        lmax = fmaxf(lmax, s);
+                    }
+                }
+            }
+        }
+        __syncthreads();   // buffer c % kNB is free
+        if (threadIdx.x == 0 && c + kNB < nseq) issue(issued_hi = c + kNB);
+    }
+    lmax = warp_max(lmax);
+    if (lane == 0) red[warp] = lmax;
+    __syncthreads();
+    float mx = red[0];
+#pragma unroll
+    for (int i = 1; i < NWARP; ++i) mx = fmaxf(mx, red[i]);
+    __syncthreads();
+    float lsum = 0.0f;
+    if (!failed) {
+        for (int j = threadIdx.x; j < L; j += kDecThreads) {
+            const float p = expf(sc[j] - mx);
+            sc[j] = p;
+            lsum += p;
+        }
+    }
+    lsum = warp_sum(lsum);
+    if (lane == 0) red[warp] = lsum;
+    __syncthreads();
+    float l = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NWARP; ++i) l += red[i];
+
+    // ---------------- pass 2: V (see decode_attn_kernel for the MMA layout)
+    float accv[8][4];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) accv[e][0] = accv[e][1] = accv[e][2] = accv[e][3] = 0.0f;
+    float s_pm = 0.0f, s_p2 = 0.0f;
+    const bool gown = g < G;
+    for (int c = 0; c < nK && !failed; ++c) {
+        const int seq = nK + c;
+        if (!wait_chunk(seq)) {
+            failed = true;
+            break;
+        }
+        const uint8_t* buf = dyn + (seq % kNB) * kChunkBytes;
+        const int r0 = c * kCK, n = chunk_n(c);
+        const int ntile = (n + 15) >> 4;
+        for (int kt = warp; kt < ntile; kt += NWARP) {
+            const int j0 = kt * 16;
+            int keys[4] = {j0 + 2 * t, j0 + 2 * t + 1, j0 + 2 * t + 8, j0 + 2 * t + 9};
+            uint32_t bw[2];
+            {
+                float pp[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const bool ok = keys[u] < n;
+                    const float p = ok ? sc[r0 + keys[u]] : 0.0f;
+                    float pv = 0.0f;
+                    if (gown && ok) {
+                        const float2 m = *reinterpret_cast<const float2*>(buf + kCKMax * RB + keys[u] * kMB128 + g * 8);
+                        pv = p * m.y;
+                        s_pm += p * m.x;
+                    }
+                    pp[u] = pv;
+                }
+                bw[0] = pack_h2(pp[0], pp[1]);
+                bw[1] = pack_h2(pp[2], pp[3]);
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&bw[0]));
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&bw[1]));
+                s_p2 += (f0.x + f0.y) + (f1.x + f1.y);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) keys[u] = min(keys[u], n - 1);
+            uint32_t w0[4], w1[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint8_t* r = buf + keys[u] * RB;
+                w0[u] = *reinterpret_cast<const uint32_t*>(r + 4 * g);
+                w1[u] = *reinterpret_cast<const uint32_t*>(r + 32 + 4 * g);
+            }
+            const uint32_t lo0 = __byte_perm(w0[0], w0[1], 0x5410), hi0 = __byte_perm(w0[0], w0[1], 0x7632);
+            const uint32_t lo2 = __byte_perm(w0[2], w0[3], 0x5410), hi2 = __byte_perm(w0[2], w0[3], 0x7632);
+            const uint32_t lo1 = __byte_perm(w1[0], w1[1], 0x5410), hi1 = __byte_perm(w1[0], w1[1], 0x7632);
+            const uint32_t lo3 = __byte_perm(w1[2], w1[3], 0x5410), hi3 = __byte_perm(w1[2], w1[3], 0x7632);
+            __syncwarp();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t a0 = nib_pair(e < 4 ? lo0 : hi0, e & 3);
+                const uint32_t a2 = nib_pair(e < 4 ? lo2 : hi2, e & 3);
+                const uint32_t a1 = nib_pair(e < 4 ? lo1 : hi1, e & 3);
+                const uint32_t a3 = nib_pair(e < 4 ? lo3 : hi3, e & 3);
+                mma16816(accv[e], a0, a1, a2, a3, bw[0], bw[1]);
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0 && seq + kNB < nseq) issue(issued_hi = seq + kNB);
+    }
+    if (failed) {
+        // no copy may land after the block leaves: wait (bounded) for every
+        // buffer's last issued chunk, then report
+        if (threadIdx.x == 0) {
+            for (int i = 0; i < kNB && i <= issued_hi; ++i) {
+                const int last = i + ((issued_hi - i) / kNB) * kNB;   // last chunk issued to buffer i
+                mbar_wait(smem_u32(&full_bar[i]), (last / kNB) & 1, nullptr, wait_ns);
+            }
+            report(status, fg::kDevTimeout);
+        }
+        return;
+    }
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+        s_pm += __shfl_xor_sync(0xffffffffu, s_pm, o);
+        s_p2 += __shfl_xor_sync(0xffffffffu, s_p2, o);
+    }
+    if (t == 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            part[warp][8 * g + e] = accv[e][0];
+            part[warp][64 + 8 * g + e] = accv[e][3];
+        }
+        if (gown) {
+            part_s[warp][g][0] = s_pm;
+            part_s[warp][g][1] = s_p2;
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < D; i += kDecThreads) {
+        const int grp = i >> 6;
+        float dsum = 0.0f, pm = 0.0f, p2 = 0.0f;
+#pragma unroll
+        for (int w = 0; w < NWARP; ++w) {
+            dsum += part[w][i];
+            pm += part_s[w][grp][0];
+            p2 += part_s[w][grp][1];
+        }
+        const float o = (pm + 16.0f * (dsum - p2)) / l;
+        out[b * h1 + static_cast<int64_t>(h) * D + i] = __float2half_rn(o);
+    }
+}
+
 // Causal prefill attention over fp16 Q/K/V.  One CTA per (32-query tile,
 // head, sequence); 4 threads per query, each owning D/4 interleaved dims
 // (dim = 4*e + part) so the 4 reads of a key row hit 4 different banks.
@@ -446,6 +762,26 @@ fg_status launch_decode_t(const __half* qkv, int64_t ld, const fg_kv4* c, int32_
     return fg::cuda_error(cudaGetLastError(), "decode_attn launch");
 }
 
+fg_status launch_decode_staged(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
+                               int32_t fuse_append, __half* out, cudaStream_t st) {
+    constexpr int D = 128;
+    const int L = pos + 1;
+    const size_t smem = static_cast<size_t>(kNB) * kChunkBytes + sizeof(float) * ((L + 3) & ~3);
+    auto kern = decode_attn_staged_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return fg::cuda_error(e, "decode_attn smem attribute");
+    dim3 grid(c->H, c->B);
+    const double row = D / 2 + (D / 64) * 8.0;
+    const double bh = static_cast<double>(c->B) * c->H;
+    fg::TraceScope ts(FG_TRACE_ATTN_DECODE, st, 4.0 * bh * L * D,
+                      bh * (2.0 * L * row + (fuse_append ? 2.0 * row : 0.0) + 3.0 * D * 2 + D * 2));
+    kern<<<grid, kDecThreads, smem, st>>>(qkv, ld, c->H, c->cap, pos, fuse_append, c->k_codes,
+                                          c->v_codes, c->k_meta, c->v_meta, out,
+                                          fg::device_status_ptr(), fg::wait_limit_ns());
+    return fg::cuda_error(cudaGetLastError(), "decode_attn launch");
+}
+
 }  // namespace
 
 namespace fg {
@@ -454,7 +790,7 @@ fg_status launch_decode_attn(const __half* qkv, int64_t ld, const fg_kv4* c, int
                              int32_t fuse_append, __half* out, cudaStream_t st) {
     if (c->B == 0) return FG_OK;
     if (c->d == 64) return launch_decode_t<64>(qkv, ld, c, pos, fuse_append, out, st);
-    return launch_decode_t<128>(qkv, ld, c, pos, fuse_append, out, st);
+    return launch_decode_staged(qkv, ld, c, pos, fuse_append, out, st);
 }
 
 fg_status launch_prefill_attn(const __half* qkv, int32_t B, int32_t s, int32_t H, int32_t d,

@@ -169,6 +169,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tm, int x,
         "l"(tm), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
+// 1-D bulk copy global -> this CTA's shared memory (both addresses 16-byte
+// aligned, size a multiple of 16), completing `bytes` of transaction count on
+// the mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+// Orders this thread's earlier generic global writes before later async-proxy
+// (TMA / bulk copy) reads of the same memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 // Multicast variant: the box lands at the same shared-memory offset in every
 // CTA of the cluster named in `mask`, completing bytes on each one's mbarrier
 // at the same offset.
