@@ -259,16 +259,24 @@ def run_fg(args, ws, rank, local):
         step()
     fg.fg_check()
 
-    # ---------------- timed region (device-resident inputs)
+    # ---------------- timed region (device-resident inputs).  K steps timed
+    # with one event pair per phase give the throughput; K more steps with an
+    # event pair around every launch of the traced kernel classes give the
+    # per-kernel durations behind the roofline (those events add a little
+    # device time, so they stay out of the throughput steps).
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     barrier()
     torch.cuda.synchronize()
     clocks.start()
+    for k in range(args.steps):
+        step(evs[k])
+    torch.cuda.synchronize()
+    barrier()
     fg.fg_trace_begin(fg.FG_TRACE_GEMM_PREFILL | fg.FG_TRACE_GEMM_DECODE |
                       fg.FG_TRACE_ATTN_DECODE | fg.FG_TRACE_ATTN_PREFILL)
     for k in range(args.steps):
-        step(evs[k])
+        step()
     torch.cuda.synchronize()
     trace = fg.fg_trace_end()
     barrier()
