@@ -436,6 +436,20 @@ def attn_case(B, H, d, L, iters, dev, seed=0):
     return sec, bytes_ / sec / 1e9
 
 
+def prefill_case(B, s, H, d, iters, dev, seed=0):
+    """One causal prefill-attention launch over fp16 Q/K/V of B sequences of s
+    tokens; returns (seconds, causal TFLOP/s)."""
+    from bit_group_quant_gb300 import fg
+    g = synth.generator(seed, dev)
+    qkv = synth.normal_f16((B * s, 3 * H * d), 1.0, g, dev)
+    out = torch.empty((B * s, H * d), dtype=torch.float16, device=dev)
+    fn = lambda: fg.fg_prefill_attn(qkv, B, s, H, d, out=out)
+    sec = _time_launches(fn, iters, torch.cuda.current_stream())
+    fg.fg_check()
+    flops = 4.0 * B * H * (s * (s + 1) / 2.0) * d
+    return sec, flops / sec / 1e12
+
+
 def run_micro(args):
     torch.cuda.set_device(0)
     dev = "cuda:0"
@@ -445,6 +459,11 @@ def run_micro(args):
         return {"micro": "dequant_gemm", "M": args.M, "N": args.N, "K": args.K,
                 "ms": sec * 1e3, "tflops": tf, "gbs": gb,
                 "frac_tensor": tf / peaks["bf16_tflops"], "peak_source": kind + " bf16_tflops"}
+    if args.micro == "prefill":
+        sec, tf = prefill_case(args.B, args.L, args.H, args.d, args.iters, dev)
+        return {"micro": "prefill_attn", "B": args.B, "s": args.L, "H": args.H, "d": args.d,
+                "ms": sec * 1e3, "tflops_causal": tf, "frac_tensor": tf / peaks["bf16_tflops"],
+                "peak_source": kind + " bf16_tflops"}
     if args.micro == "attn":
         sec, gb = attn_case(args.B, args.H, args.d, args.L, args.iters, dev)
         return {"micro": "decode_attn_g4", "B": args.B, "H": args.H, "d": args.d, "L": args.L,
@@ -523,7 +542,7 @@ def main(argv=None):
     ap.add_argument("--ref-frac", type=int, default=4)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--micro", choices=["gemm", "attn", "sweep175b"], default=None,
+    ap.add_argument("--micro", choices=["gemm", "attn", "prefill", "sweep175b"], default=None,
                     help="time one kernel shape (or the OPT-175B layer sweep) instead")
     ap.add_argument("--M", type=int, default=4096)
     ap.add_argument("--N", type=int, default=28672)
