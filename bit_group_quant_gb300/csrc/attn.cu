@@ -36,8 +36,11 @@ __device__ __forceinline__ float warp_sum(float v) {
 //   sum_j p_j v^_j[i] = sum_j p_j m_{j,g} + sum_j (p_j s_{j,g}) c_{j,i}
 // so (min, scale) apply once per key and group, and the code dot products run
 // on the tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate) with the
-// codes encoded exactly as fp16 1 + c/16 (one shift and one LOP3 per pair of
-// codes); sum (1 + c/16) x = sum x + (1/16) sum c x removes the offset.
+// codes masked in place as fp16 subnormals c * 2^-24 (16 c * 2^-24 for odd
+// nibble pairs, compensated by q / 16 in the other operand or by 1/16 at the
+// end): one AND per pair of codes, and sum x c = 2^24 times the MMA sum, with
+// no offset term whose cancellation the tensor cores' accumulation would
+// blur.
 //
 // One CTA (4 warps) per (head, sequence); warps take 16-key tiles in turn.
 // Pass 1: scores of all L keys into shared memory.  Then the exact maximum
@@ -54,10 +57,14 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// half2(1 + c_e/16, 1 + c_{e+4}/16) from nibbles e and e+4 of w (e in 0..3).
-__device__ __forceinline__ uint32_t nib_pair(uint32_t w, int e) {
-    const uint32_t sh = e == 0 ? (w << 6) : e == 1 ? (w << 2) : e == 2 ? (w >> 2) : (w >> 6);
-    return (sh & 0x03C003C0u) | 0x3C003C00u;
+// half2 codes of nibble pair (p, p+4) of word w in the staged kernel's
+// encoding: masked in place as fp16 subnormals, c * 2^-24 for even p and
+// 16 c * 2^-24 for odd p (p = 2, 3 read from w >> 8) -- one AND per pair
+// plus one shift per word.  No offset term: the tensor cores sum the
+// products q * c * 2^-24 without a large common part to cancel.
+__device__ __forceinline__ uint32_t enc_pair(uint32_t w, uint32_t w8, int p) {
+    const uint32_t src = p < 2 ? w : w8;
+    return src & ((p & 1) ? 0x00F000F0u : 0x000F000Fu);
 }
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
@@ -158,7 +165,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
             const float q1 = use ? __half2float(qrow[base + 1]) : 0.0f;
             const float q5 = use ? __half2float(qrow[base + 5]) : 0.0f;
             qb[x][0] = pack_h2(q0, q4);
-            qb[x][1] = pack_h2(q1, q5);
+            qb[x][1] = pack_h2(q1 * 0.0625f, q5 * 0.0625f);   // exact: pairs e+1 carry 16 c
         }
     }
     __syncthreads();
@@ -185,13 +192,21 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
             wa[0] = va.x; wa[1] = va.y;
             wb[0] = vb.x; wb[1] = vb.y;
         }
+        uint32_t wa8[WPT], wb8[WPT];
+#pragma unroll
+        for (int i = 0; i < WPT; ++i) {
+            wa8[i] = wa[i] >> 8;
+            wb8[i] = wb[i] >> 8;
+        }
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         __syncwarp();   // mma.sync is .aligned: reconverge after last round's lane-0 work
 #pragma unroll
         for (int x = 0; x < NX; ++x) {
             const int e = 2 * (x & 1);
-            mma16816(acc, nib_pair(wa[x >> 1], e), nib_pair(wb[x >> 1], e),
-                     nib_pair(wa[x >> 1], e + 1), nib_pair(wb[x >> 1], e + 1), qb[x][0], qb[x][1]);
+            const int wi = x >> 1;
+            mma16816(acc, enc_pair(wa[wi], wa8[wi], e), enc_pair(wb[wi], wb8[wi], e),
+                     enc_pair(wa[wi], wa8[wi], e + 1), enc_pair(wb[wi], wb8[wi], e + 1),
+                     qb[x][0], qb[x][1]);
         }
         if (t == 0) {
             // acc: (key g, group 0), (key g, group 1), (key g+8, group 0), (key g+8, group 1)
@@ -201,13 +216,14 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
                 if (j < L) {
                     const float* km = k_meta + (row0 + j) * G * 2;
                     float dot;
+                    // sum q c = 2^24 acc per group
                     if (G == 2) {
                         const float4 m = *reinterpret_cast<const float4*>(km);
-                        dot = m.x * Q0 + 16.0f * m.y * (acc[2 * half] - Q0) +
-                              m.z * Q1 + 16.0f * m.w * (acc[2 * half + 1] - Q1);
+                        dot = m.x * Q0 + 16777216.0f * m.y * acc[2 * half] +
+                              m.z * Q1 + 16777216.0f * m.w * acc[2 * half + 1];
                     } else {
                         const float2 m = *reinterpret_cast<const float2*>(km);
-                        dot = m.x * Q0 + 16.0f * m.y * (acc[2 * half] - Q0);
+                        dot = m.x * Q0 + 16777216.0f * m.y * acc[2 * half];
                     }
                     const float s = dot * attn_scale;
                     sc[j] = s;
@@ -242,7 +258,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
     float accv[8][4];
 #pragma unroll
     for (int e = 0; e < 8; ++e) accv[e][0] = accv[e][1] = accv[e][2] = accv[e][3] = 0.0f;
-    float s_pm = 0.0f, s_p2 = 0.0f;   // this lane's keys: sum p m, sum p' (group g)
+    float s_pm = 0.0f;   // this lane's keys: sum p * min (group g)
     const bool gown = g < G;
     for (int kt = warp; kt < ntile; kt += NWARP) {
         const int j0 = kt * 16;
@@ -265,9 +281,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
             }
             bw[0] = pack_h2(pp[0], pp[1]);
             bw[1] = pack_h2(pp[2], pp[3]);
-            const float2 r0 = __half22float2(*reinterpret_cast<const __half2*>(&bw[0]));
-            const float2 r1 = __half22float2(*reinterpret_cast<const __half2*>(&bw[1]));
-            s_p2 += (r0.x + r0.y) + (r1.x + r1.y);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) keys[u] = min(keys[u], L - 1);
@@ -284,50 +297,50 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
         const uint32_t lo2 = __byte_perm(w0[2], w0[3], 0x5410), hi2 = __byte_perm(w0[2], w0[3], 0x7632);
         const uint32_t lo1 = __byte_perm(w1[0], w1[1], 0x5410), hi1 = __byte_perm(w1[0], w1[1], 0x7632);
         const uint32_t lo3 = __byte_perm(w1[2], w1[3], 0x5410), hi3 = __byte_perm(w1[2], w1[3], 0x7632);
+        const uint32_t lo0s = lo0 >> 8, hi0s = hi0 >> 8, lo1s = lo1 >> 8, hi1s = hi1 >> 8;
+        const uint32_t lo2s = lo2 >> 8, hi2s = hi2 >> 8, lo3s = lo3 >> 8, hi3s = hi3 >> 8;
         __syncwarp();   // mma.sync is .aligned: reconverge after the per-key loads above
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const uint32_t a0 = nib_pair(e < 4 ? lo0 : hi0, e & 3);
-            const uint32_t a2 = nib_pair(e < 4 ? lo2 : hi2, e & 3);
-            const uint32_t a1 = (D == 128) ? nib_pair(e < 4 ? lo1 : hi1, e & 3) : 0u;
-            const uint32_t a3 = (D == 128) ? nib_pair(e < 4 ? lo3 : hi3, e & 3) : 0u;
+            const int p = e & 3;   // MMA e: codes k_e c 2^-24, k_e = 16 for odd e
+            const uint32_t a0 = e < 4 ? enc_pair(lo0, lo0s, p) : enc_pair(hi0, hi0s, p);
+            const uint32_t a2 = e < 4 ? enc_pair(lo2, lo2s, p) : enc_pair(hi2, hi2s, p);
+            const uint32_t a1 = (D == 128) ? (e < 4 ? enc_pair(lo1, lo1s, p) : enc_pair(hi1, hi1s, p)) : 0u;
+            const uint32_t a3 = (D == 128) ? (e < 4 ? enc_pair(lo3, lo3s, p) : enc_pair(hi3, hi3s, p)) : 0u;
             mma16816(accv[e], a0, a1, a2, a3, bw[0], bw[1]);
         }
     }
     // group sums of this warp: reduce over the 4 lanes (g, t) of each group
 #pragma unroll
-    for (int o = 1; o < 4; o <<= 1) {
-        s_pm += __shfl_xor_sync(0xffffffffu, s_pm, o);
-        s_p2 += __shfl_xor_sync(0xffffffffu, s_p2, o);
-    }
+    for (int o = 1; o < 4; o <<= 1) s_pm += __shfl_xor_sync(0xffffffffu, s_pm, o);
     if (t == 0) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             part[warp][8 * g + e] = accv[e][0];                 // group 0 dims x p'(group 0)
             if (D == 128) part[warp][64 + 8 * g + e] = accv[e][3];  // group 1 dims x p'(group 1)
         }
-        if (gown) {
-            part_s[warp][g][0] = s_pm;
-            part_s[warp][g][1] = s_p2;
-        }
+        if (gown) part_s[warp][g][0] = s_pm;
     }
     __syncthreads();
     for (int i = threadIdx.x; i < D; i += kDecThreads) {
         const int grp = i >> 6;
-        float dsum = 0.0f, pm = 0.0f, p2 = 0.0f;
+        float dsum = 0.0f, pm = 0.0f;
 #pragma unroll
         for (int w = 0; w < NWARP; ++w) {
             dsum += part[w][i];
             pm += part_s[w][grp][0];
-            p2 += part_s[w][grp][1];
         }
-        const float o = (pm + 16.0f * (dsum - p2)) / l;
+        // dim i comes from MMA e = i % 8: sum (p s) c = 2^24 / k_e acc, k_e = 16 for odd e
+        const float kinv = (i & 1) ? 1048576.0f : 16777216.0f;
+        const float o = (pm + kinv * dsum) / l;
         out[b * h1 + static_cast<int64_t>(h) * D + i] = __float2half_rn(o);
     }
 }
 
 // Decode attention for d = 128 with the cache streamed through shared memory.
-// Same arithmetic as decode_attn_kernel; the data path differs: for one
+// The same per-group algebra as decode_attn_kernel, but the codes enter the
+// MMAs as fp16 subnormals c * 2^-24 (one AND per pair of codes, no offset to
+// cancel), so sum q c = 2^24 acc and sum (p s) c = 2^24 acc / k.  For one
 // (head, sequence) the L cached rows of K codes, K (min, scale), V codes and
 // V (min, scale) are four contiguous regions, fetched in chunks of kCK rows by
 // 1-D bulk asynchronous copies (the async proxy) into a ring of kNB chunk
@@ -358,6 +371,7 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     __shared__ float red[NWARP];
     __shared__ float part[NWARP][D];
     __shared__ float part_s[NWARP][2][2];
+    __shared__ int fail_sh;
 
     const int h = blockIdx.x, b = blockIdx.y;
     const int L = pos + 1;
@@ -426,6 +440,7 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNB; ++i) mbar_init(smem_u32(&full_bar[i]), 1);
         fence_mbar_init();
+        fail_sh = 0;
     }
     // q as the B operand of the pass-1 MMAs (see decode_attn_kernel)
     uint32_t qb[NX][2];
@@ -440,7 +455,7 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
             const float q1 = use ? __half2float(qrow[base + 1]) : 0.0f;
             const float q5 = use ? __half2float(qrow[base + 5]) : 0.0f;
             qb[x][0] = pack_h2(q0, q4);
-            qb[x][1] = pack_h2(q1, q5);
+            qb[x][1] = pack_h2(q1 * 0.0625f, q5 * 0.0625f);   // exact: pairs e+1 carry 16 c
         }
     }
     __syncthreads();
@@ -460,10 +475,15 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     int issued_hi = -1;   // thread 0: highest chunk seq issued so far
     if (threadIdx.x == 0)
         for (int i = 0; i < kNB && i < nseq; ++i) issue(issued_hi = i);
-    // bounded wait for chunk seq, made uniform over the block; false = give up
+    // Bounded wait for chunk seq, made uniform over the warp (the MMAs are
+    // warp-synchronous); a warp that gives up raises fail_sh, which every
+    // thread reads after the block barrier that ends the chunk.  One block
+    // barrier per chunk: it also frees the buffer for the next copy.
     auto wait_chunk = [&](int seq) {
-        const bool ok = mbar_wait(smem_u32(&full_bar[seq % kNB]), (seq / kNB) & 1, nullptr, wait_ns);
-        return __syncthreads_and(ok ? 1 : 0) != 0;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[seq % kNB]),
+                                                          (seq / kNB) & 1, nullptr, wait_ns));
+        if (!ok && lane == 0) fail_sh = 1;
+        return ok;
     };
     bool failed = false;
 
@@ -472,27 +492,32 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
 
     // ---------------- pass 1: scores
     float lmax = -CUDART_INF_F;
-    for (int c = 0; c < nK && !failed; ++c) {
-        if (!wait_chunk(c)) {
-            failed = true;
-            break;
-        }
+    for (int c = 0; c < nK; ++c) {
+        const bool ok = wait_chunk(c);
         const uint8_t* buf = dyn + (c % kNB) * kChunkBytes;
         const int r0 = c * kCK, n = chunk_n(c);
-        const int ntile = (n + 15) >> 4;
+        const int ntile = ok ? (n + 15) >> 4 : 0;
         for (int kt = warp; kt < ntile; kt += NWARP) {
             const int ja = min(kt * 16 + g, n - 1), jb = min(kt * 16 + g + 8, n - 1);
             const uint4 va = *reinterpret_cast<const uint4*>(buf + ja * RB + t * 16);
             const uint4 vb = *reinterpret_cast<const uint4*>(buf + jb * RB + t * 16);
             const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
             const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
+            uint32_t wa8[4], wb8[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                wa8[i] = wa[i] >> 8;
+                wb8[i] = wb[i] >> 8;
+            }
             float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             __syncwarp();
 #pragma unroll
             for (int x = 0; x < NX; ++x) {
                 const int e = 2 * (x & 1);
-                mma16816(acc, nib_pair(wa[x >> 1], e), nib_pair(wb[x >> 1], e),
-                         nib_pair(wa[x >> 1], e + 1), nib_pair(wb[x >> 1], e + 1), qb[x][0], qb[x][1]);
+                const int wi = x >> 1;
+                mma16816(acc, enc_pair(wa[wi], wa8[wi], e), enc_pair(wb[wi], wb8[wi], e),
+                         enc_pair(wa[wi], wa8[wi], e + 1), enc_pair(wb[wi], wb8[wi], e + 1),
+                         qb[x][0], qb[x][1]);
             }
             if (t == 0) {
 #pragma unroll
@@ -500,8 +525,9 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
                     const int jl = kt * 16 + g + 8 * half;
                     if (jl < n) {
                         const float4 m = *reinterpret_cast<const float4*>(buf + kCKMax * RB + jl * kMB128);
-                        const float dot = m.x * Q0 + 16.0f * m.y * (acc[2 * half] - Q0) +
-                                          m.z * Q1 + 16.0f * m.w * (acc[2 * half + 1] - Q1);
+                        // sum q c = 2^24 acc per group
+                        const float dot = m.x * Q0 + 16777216.0f * m.y * acc[2 * half] +
+                                          m.z * Q1 + 16777216.0f * m.w * acc[2 * half + 1];
                         const float s = dot * attn_scale;
                         sc[r0 + jl] = s;
                         lmax = fmaxf(lmax, s);
@@ -509,7 +535,11 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
                 }
             }
         }
-        __syncthreads();   // buffer c % kNB is free
+        __syncthreads();   // buffer c % kNB is free; fail_sh visible
+        if (fail_sh) {
+            failed = true;
+            break;
+        }
         if (threadIdx.x == 0 && c + kNB < nseq) issue(issued_hi = c + kNB);
     }
     lmax = warp_max(lmax);
@@ -538,17 +568,14 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     float accv[8][4];
 #pragma unroll
     for (int e = 0; e < 8; ++e) accv[e][0] = accv[e][1] = accv[e][2] = accv[e][3] = 0.0f;
-    float s_pm = 0.0f, s_p2 = 0.0f;
+    float s_pm = 0.0f;   // this lane's keys: sum p * min (group g)
     const bool gown = g < G;
     for (int c = 0; c < nK && !failed; ++c) {
         const int seq = nK + c;
-        if (!wait_chunk(seq)) {
-            failed = true;
-            break;
-        }
+        const bool ok = wait_chunk(seq);
         const uint8_t* buf = dyn + (seq % kNB) * kChunkBytes;
         const int r0 = c * kCK, n = chunk_n(c);
-        const int ntile = (n + 15) >> 4;
+        const int ntile = ok ? (n + 15) >> 4 : 0;
         for (int kt = warp; kt < ntile; kt += NWARP) {
             const int j0 = kt * 16;
             int keys[4] = {j0 + 2 * t, j0 + 2 * t + 1, j0 + 2 * t + 8, j0 + 2 * t + 9};
@@ -569,9 +596,6 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
                 }
                 bw[0] = pack_h2(pp[0], pp[1]);
                 bw[1] = pack_h2(pp[2], pp[3]);
-                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&bw[0]));
-                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&bw[1]));
-                s_p2 += (f0.x + f0.y) + (f1.x + f1.y);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) keys[u] = min(keys[u], n - 1);
@@ -587,16 +611,23 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
             const uint32_t lo1 = __byte_perm(w1[0], w1[1], 0x5410), hi1 = __byte_perm(w1[0], w1[1], 0x7632);
             const uint32_t lo3 = __byte_perm(w1[2], w1[3], 0x5410), hi3 = __byte_perm(w1[2], w1[3], 0x7632);
             __syncwarp();
+            const uint32_t lo0s = lo0 >> 8, hi0s = hi0 >> 8, lo1s = lo1 >> 8, hi1s = hi1 >> 8;
+            const uint32_t lo2s = lo2 >> 8, hi2s = hi2 >> 8, lo3s = lo3 >> 8, hi3s = hi3 >> 8;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const uint32_t a0 = nib_pair(e < 4 ? lo0 : hi0, e & 3);
-                const uint32_t a2 = nib_pair(e < 4 ? lo2 : hi2, e & 3);
-                const uint32_t a1 = nib_pair(e < 4 ? lo1 : hi1, e & 3);
-                const uint32_t a3 = nib_pair(e < 4 ? lo3 : hi3, e & 3);
+                const int p = e & 3;   // MMA e: codes 1 + k_e c 2^-10, k_e = 16 for odd e
+                const uint32_t a0 = e < 4 ? enc_pair(lo0, lo0s, p) : enc_pair(hi0, hi0s, p);
+                const uint32_t a2 = e < 4 ? enc_pair(lo2, lo2s, p) : enc_pair(hi2, hi2s, p);
+                const uint32_t a1 = e < 4 ? enc_pair(lo1, lo1s, p) : enc_pair(hi1, hi1s, p);
+                const uint32_t a3 = e < 4 ? enc_pair(lo3, lo3s, p) : enc_pair(hi3, hi3s, p);
                 mma16816(accv[e], a0, a1, a2, a3, bw[0], bw[1]);
             }
         }
-        __syncthreads();
+        __syncthreads();   // buffer free; fail_sh visible
+        if (fail_sh) {
+            failed = true;
+            break;
+        }
         if (threadIdx.x == 0 && seq + kNB < nseq) issue(issued_hi = seq + kNB);
     }
     if (failed) {
@@ -612,32 +643,27 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
         return;
     }
 #pragma unroll
-    for (int o = 1; o < 4; o <<= 1) {
-        s_pm += __shfl_xor_sync(0xffffffffu, s_pm, o);
-        s_p2 += __shfl_xor_sync(0xffffffffu, s_p2, o);
-    }
+    for (int o = 1; o < 4; o <<= 1) s_pm += __shfl_xor_sync(0xffffffffu, s_pm, o);
     if (t == 0) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             part[warp][8 * g + e] = accv[e][0];
             part[warp][64 + 8 * g + e] = accv[e][3];
         }
-        if (gown) {
-            part_s[warp][g][0] = s_pm;
-            part_s[warp][g][1] = s_p2;
-        }
+        if (gown) part_s[warp][g][0] = s_pm;
     }
     __syncthreads();
     for (int i = threadIdx.x; i < D; i += kDecThreads) {
         const int grp = i >> 6;
-        float dsum = 0.0f, pm = 0.0f, p2 = 0.0f;
+        float dsum = 0.0f, pm = 0.0f;
 #pragma unroll
         for (int w = 0; w < NWARP; ++w) {
             dsum += part[w][i];
             pm += part_s[w][grp][0];
-            p2 += part_s[w][grp][1];
         }
-        const float o = (pm + 16.0f * (dsum - p2)) / l;
+        // dim i comes from MMA e = i % 8: sum (p s) c = 2^24 / k_e acc, k_e = 16 for odd e
+        const float kinv = (i & 1) ? 1048576.0f : 16777216.0f;
+        const float o = (pm + kinv * dsum) / l;
         out[b * h1 + static_cast<int64_t>(h) * D + i] = __float2half_rn(o);
     }
 }
