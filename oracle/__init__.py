@@ -84,8 +84,9 @@ def _load():
                 "or_layernorm": ([P, I64, I64, P, P, F, P], None),
                 "or_embed": ([P, P, I64, P, P, I64, P], None),
                 "or_kv_store_prefill": ([P, I32, I32, P, P, P, P, I32, I32, I32], None),
-                "or_prefill_attn": ([P, I32, I32, I32, I32, P], None),
-                "or_decode_attn_g4": ([P, I64, P, P, P, P, I32, I32, I32, I32, I32, I32, P], None),
+                "or_prefill_attn": ([P, I32, I32, I32, I32, P, P], None),
+                "or_decode_attn_g4": ([P, I64, P, P, P, P, I32, I32, I32, I32, I32, I32, P, P], None),
+                "or_argmax": ([P, I64, I64, P], None),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -269,24 +270,45 @@ def kv_store_prefill(qkv, B, s, cache: KVCache):
                                 cache.d, cache.cap)
 
 
-def prefill_attn(qkv, B, s, H, d):
+def _pad(pad, B):
+    if pad is None:
+        return None
+    pad = _c(pad, np.int32).reshape(-1)
+    assert pad.size == B
+    return pad
+
+
+def prefill_attn(qkv, B, s, H, d, pad=None):
+    """pad: None or [B] left-padding counts (prompt b fills slots pad[b]..s-1)."""
     qkv = _c(qkv, np.float16)
     assert qkv.shape == (B * s, 3 * H * d)
     out = np.empty((B * s, H * d), np.float16)
-    _load().or_prefill_attn(_p(qkv), B, s, H, d, _p(out))
+    pad = _pad(pad, B)
+    _load().or_prefill_attn(_p(qkv), B, s, H, d, None if pad is None else _p(pad), _p(out))
     return out
 
 
-def decode_attn_g4(qkv, cache: KVCache, pos, append=True):
-    """qkv: [B][>=3*h1] fp16 (row stride = qkv.shape[1])."""
+def decode_attn_g4(qkv, cache: KVCache, pos, append=True, pad=None):
+    """qkv: [B][>=3*h1] fp16 (row stride = qkv.shape[1]); pad: None or [B]
+    left-padding counts (sequence b attends slots pad[b]..pos)."""
     qkv = _c(qkv, np.float16)
     B = qkv.shape[0]
     assert B == cache.B and 0 <= pos < cache.cap
     out = np.empty((B, cache.H * cache.d), np.float16)
     kc, vc, km, vm = cache._ptrs()
+    pad = _pad(pad, B)
     _load().or_decode_attn_g4(_p(qkv), qkv.shape[1], kc, vc, km, vm, cache.B,
                               cache.H, cache.d, cache.cap, int(pos),
-                              1 if append else 0, _p(out))
+                              1 if append else 0, None if pad is None else _p(pad), _p(out))
+    return out
+
+
+def argmax(logits):
+    """Greedy token per row of fp32 logits [B][V] (lowest index among ties)."""
+    logits = _c(logits, np.float32)
+    B, V = logits.shape
+    out = np.empty(B, np.int32)
+    _load().or_argmax(_p(logits), B, V, _p(out))
     return out
 
 

@@ -402,9 +402,12 @@ static void softmax_weighted(const float* sc, const float* vrows, int64_t n,
 
 /* Causal prefill attention over fp16 Q/K/V taken straight from the QKV
  * projection (not yet stored, so not quantised).
- * qkv: [B*s][3*h1]; out: [B*s][h1]; score = (q . k) * (1/sqrt(d)). */
+ * qkv: [B*s][3*h1]; out: [B*s][h1]; score = (q . k) * (1/sqrt(d)).
+ * pad: NULL, or [B] left-padding counts: sequence b's prompt fills slots
+ * pad[b]..s-1, a query at slot i >= pad[b] attends keys pad[b]..i, and a
+ * query in a padding slot outputs zeros. */
 void or_prefill_attn(const uint16_t* qkv, int32_t B, int32_t s, int32_t H,
-                     int32_t d, uint16_t* out)
+                     int32_t d, const int32_t* pad, uint16_t* out)
 {
     int64_t h1 = (int64_t)H * d, ld = 3 * h1;
     float scale = 1.0f / sqrtf((float)d);
@@ -419,17 +422,22 @@ void or_prefill_attn(const uint16_t* qkv, int32_t B, int32_t s, int32_t H,
         for (int64_t b = 0; b < B; ++b)
             for (int64_t h = 0; h < H; ++h)
                 for (int64_t i = 0; i < s; ++i) {
+                    const int64_t p0 = pad ? pad[b] : 0;
+                    uint16_t* o = out + (b * s + i) * h1 + h * d;
+                    if (i < p0) {   /* padding slot */
+                        for (int64_t c = 0; c < d; ++c) o[c] = 0;
+                        continue;
+                    }
                     or_h2f_array(qkv + (b * s + i) * ld + h * d, q, d);
-                    for (int64_t j = 0; j <= i; ++j) {
+                    for (int64_t j = p0; j <= i; ++j) {
                         or_h2f_array(qkv + (b * s + j) * ld + h1 + h * d, kr, d);
                         float dot = 0.0f;
                         for (int64_t c = 0; c < d; ++c) dot += q[c] * kr[c];
-                        sc[j] = dot * scale;
+                        sc[j - p0] = dot * scale;
                         or_h2f_array(qkv + (b * s + j) * ld + 2 * h1 + h * d,
-                                     vr + j * d, d);
+                                     vr + (j - p0) * d, d);
                     }
-                    softmax_weighted(sc, vr, i + 1, d, p,
-                                     out + (b * s + i) * h1 + h * d);
+                    softmax_weighted(sc, vr, i + 1 - p0, d, p, o);
                 }
         free(q);
         free(kr);
@@ -441,12 +449,14 @@ void or_prefill_attn(const uint16_t* qkv, int32_t B, int32_t s, int32_t H,
 
 /* Decode attention over the 4-bit cache.  qkv: [B][qkv_ld] fp16 rows, one
  * new token per sequence.  If do_append, the new k and v are first quantised
- * into slot pos; then the query attends over slots 0..pos, every row (the
- * new one included) read through dequantisation.  out: [B][h1] fp16. */
+ * into slot pos; then the query attends over slots pad[b]..pos (pad NULL:
+ * 0..pos), every row (the new one included) read through dequantisation.
+ * out: [B][h1] fp16. */
 void or_decode_attn_g4(const uint16_t* qkv, int64_t qkv_ld, uint8_t* k_codes,
                        uint8_t* v_codes, float* k_meta, float* v_meta,
                        int32_t B, int32_t H, int32_t d, int32_t cap,
-                       int32_t pos, int32_t do_append, uint16_t* out)
+                       int32_t pos, int32_t do_append, const int32_t* pad,
+                       uint16_t* out)
 {
     or_kv4 c = {k_codes, v_codes, k_meta, v_meta, B, H, d, cap};
     int64_t h1 = (int64_t)H * d, L = (int64_t)pos + 1;
@@ -464,20 +474,34 @@ void or_decode_attn_g4(const uint16_t* qkv, int64_t qkv_ld, uint8_t* k_codes,
 #pragma omp for collapse(2) schedule(static)
         for (int64_t b = 0; b < B; ++b)
             for (int64_t h = 0; h < H; ++h) {
+                const int64_t p0 = pad ? pad[b] : 0;
                 or_h2f_array(qkv + b * qkv_ld + h * d, q, d);
-                for (int64_t j = 0; j < L; ++j) {
+                for (int64_t j = p0; j < L; ++j) {
                     load_cache_row(&c, 0, b, h, j, kr);
                     float dot = 0.0f;
                     for (int64_t i = 0; i < d; ++i) dot += q[i] * kr[i];
-                    sc[j] = dot * scale;
-                    load_cache_row(&c, 1, b, h, j, vr + j * d);
+                    sc[j - p0] = dot * scale;
+                    load_cache_row(&c, 1, b, h, j, vr + (j - p0) * d);
                 }
-                softmax_weighted(sc, vr, L, d, p, out + b * h1 + h * d);
+                softmax_weighted(sc, vr, L - p0, d, p, out + b * h1 + h * d);
             }
         free(q);
         free(kr);
         free(sc);
         free(p);
         free(vr);
+    }
+}
+
+/* Greedy choice: for each of B rows of V fp32 logits, the index of the
+ * largest value (the lowest such index when several are equal). */
+void or_argmax(const float* logits, int64_t B, int64_t V, int32_t* out)
+{
+    for (int64_t b = 0; b < B; ++b) {
+        const float* r = logits + b * V;
+        int64_t best = 0;
+        for (int64_t v = 1; v < V; ++v)
+            if (r[v] > r[best]) best = v;
+        out[b] = (int32_t)best;
     }
 }

@@ -17,6 +17,18 @@ plain C primitives of this package; the composition follows the pages:
   Batches are independent, so all orders must give identical results.
 * The first generated token comes out of the prefill, so n generated tokens
   take n-1 decode steps (T = l*T_pre + l*(n-1)*T_gen on the same page).
+* Prompts of different lengths share one block by left padding to the
+  common length s (the pages' workloads pad every prompt to 512 or 1024,
+  "FlexGen 完全拆解", section on reading the
+  experimental results).  The pages do not spell the
+  masking out; the reading taken here: prompt b occupies slots pad[b]..s-1,
+  its tokens take positions 0..s-1-pad[b] (decode step t: position
+  s+t-1-pad[b]), every query attends only keys at slots >= pad[b] (and, in
+  the prefill, <= its own slot), and queries in padding slots give zero
+  attention output.  A padded prompt then yields exactly the results of the
+  same prompt run unpadded.
+* Greedy generation: the next token is the argmax of the logits, the lowest
+  index among equal maxima.
 * Size formulas on the same page: M_W = l(8 h1^2 + 4 h1 h2) bytes of fp16
   weights (embeddings ignored) and M_KV = 4 b l h1 (s + n) bytes of fp16 KV.
 """
@@ -26,7 +38,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from . import (GROUP, KVCache, decode_attn_g4, embed, kv_store_prefill,
+from . import (GROUP, KVCache, argmax, decode_attn_g4, embed, kv_store_prefill,
                layernorm, linear_f16_f32out, linear_g4, prefill_attn,
                quantize_g4)
 
@@ -96,20 +108,21 @@ def quantize_layer(w: dict, h1: int, H: int, h2: int, eps: float = 1e-5) -> Orac
 
 
 def layer_step(L: OracleLayer, x, cache: KVCache, phase: int, B: int, T: int,
-               pos: int = 0, trace: dict | None = None):
+               pos: int = 0, trace: dict | None = None, pad=None):
     """One decoder layer for B sequences of T new tokens each.
 
-    x: fp16 [B*T][h1] (sequence-major rows).  PREFILL: T = s prompt tokens at
-    positions 0..s-1.  DECODE: T = 1, the new token sits at cache slot pos.
+    x: fp16 [B*T][h1] (sequence-major rows).  PREFILL: T = s prompt tokens in
+    slots 0..s-1.  DECODE: T = 1, the new token sits at cache slot pos.
+    pad: None or [B] left-padding counts (attention sees slots >= pad[b]).
     """
     a = layernorm(x, L.ln1_g, L.ln1_b, L.eps)
     qkv = linear_g4(a, *L.qkv, bias=L.b_qkv)
     if phase == PREFILL:
-        attn = prefill_attn(qkv, B, T, L.H, L.d)
+        attn = prefill_attn(qkv, B, T, L.H, L.d, pad=pad)
         kv_store_prefill(qkv, B, T, cache)
     else:
         assert T == 1
-        attn = decode_attn_g4(qkv, cache, pos, append=True)
+        attn = decode_attn_g4(qkv, cache, pos, append=True, pad=pad)
     h = linear_g4(attn, *L.out, bias=L.b_out, residual=x)
     u = linear_g4(layernorm(h, L.ln2_g, L.ln2_b, L.eps), *L.fc1, bias=L.b_fc1, act=1)
     y = linear_g4(u, *L.fc2, bias=L.b_fc2, residual=h)
@@ -150,24 +163,54 @@ def _embed_rows(m: OracleModel, ids, positions):
     return embed(ids, positions, m.e_tok, m.e_pos)
 
 
+def positions_of(slots, pad_b: int):
+    """Positions of a sequence's slots under left padding by pad_b (padding
+    slots take position 0; nothing real reads them)."""
+    return np.maximum(np.asarray(slots, np.int64) - pad_b, 0).astype(np.int32)
+
+
 def generate(m: OracleModel, prompt_ids, decode_ids, gbs: int, k: int,
-             order: str = "zigzag", caches=None):
+             order: str = "zigzag", caches=None, pad=None):
     """Teacher-forced generation of a block of bls = gbs*k sequences.
 
     prompt_ids: int [bls][s]; decode_ids: int [bls][D] fed at decode steps
-    1..D (position s+t-1).  Returns the list of fp32 logits [bls][V]: entry 0
-    from the prefill's last position, entry t from decode step t.
+    1..D (slot s+t-1).  pad: None or int [bls] left-padding counts (prompt b
+    is prompt_ids[b, pad[b]:]).  Returns the list of fp32 logits [bls][V]:
+    entry 0 from the prefill's last slot, entry t from decode step t.
 
     order: "row" (one GPU batch through all layers and tokens, then the next),
     "zigzag" (per token step and layer, the k batches in turn, direction
     reversed on odd token steps) or "block" (per token step and layer, one
     call over all bls rows).  All three give identical logits.
     """
-    prompt_ids = np.asarray(prompt_ids, np.int32)
     decode_ids = np.asarray(decode_ids, np.int32)
-    bls, s = prompt_ids.shape
     D = decode_ids.shape[1]
+    return _run(m, prompt_ids, D, lambda t, prev, b0, b1: decode_ids[b0:b1, t - 1],
+                gbs, k, order, caches, pad)
+
+
+def generate_greedy(m: OracleModel, prompt_ids, n_new: int, gbs: int, k: int,
+                    order: str = "zigzag", caches=None, pad=None):
+    """Greedy generation of n_new tokens per sequence: token 1 is the argmax
+    of the prefill's logits, token t+1 the argmax of decode step t's logits
+    (fed back at step t).  Returns (tokens int32 [bls][n_new], logits list as
+    generate() gives it)."""
+    assert n_new >= 1
+    out = _run(m, prompt_ids, n_new - 1, lambda t, prev, b0, b1: argmax(prev[b0:b1]),
+               gbs, k, order, caches, pad)
+    toks = np.stack([argmax(lg) for lg in out], axis=1).astype(np.int32)
+    return toks, out
+
+
+def _run(m: OracleModel, prompt_ids, D: int, ids_for_step, gbs: int, k: int,
+         order: str, caches, pad):
+    """Shared driver: ids_for_step(t, logits of step t-1, b0, b1) gives the
+    ids of sequences [b0, b1) at decode step t."""
+    prompt_ids = np.asarray(prompt_ids, np.int32)
+    bls, s = prompt_ids.shape
     assert bls == gbs * k
+    pad = np.zeros(bls, np.int32) if pad is None else np.asarray(pad, np.int32)
+    assert pad.shape == (bls,) and np.all((pad >= 0) & (pad < s))
     cap = s + D + 1
     if caches is None:
         caches = m.new_caches(bls, cap)
@@ -177,12 +220,12 @@ def generate(m: OracleModel, prompt_ids, decode_ids, gbs: int, k: int,
 
     def prefill_rows(b0, b1):
         ids = prompt_ids[b0:b1].reshape(-1)
-        pos = np.tile(np.arange(s, dtype=np.int32), b1 - b0)
+        pos = np.concatenate([positions_of(np.arange(s), pad[b]) for b in range(b0, b1)])
         return _embed_rows(m, ids, pos)
 
     def decode_rows(b0, b1, t):
-        ids = decode_ids[b0:b1, t - 1]
-        pos = np.full(b1 - b0, s + t - 1, np.int32)
+        ids = np.asarray(ids_for_step(t, out[t - 1], b0, b1), np.int32)
+        pos = np.array([s + t - 1 - pad[b] for b in range(b0, b1)], np.int32)
         return _embed_rows(m, ids, pos)
 
     def last_rows(x, nb):
@@ -190,15 +233,17 @@ def generate(m: OracleModel, prompt_ids, decode_ids, gbs: int, k: int,
 
     if order == "row":
         for (b0, b1) in batches:
+            pb = pad[b0:b1]
             x = prefill_rows(b0, b1)
             for j in range(nl):
-                x = layer_step(m.layers[j], x, caches[j].view(b0, b1), PREFILL, b1 - b0, s)
+                x = layer_step(m.layers[j], x, caches[j].view(b0, b1), PREFILL, b1 - b0, s,
+                               pad=pb)
             out[0][b0:b1] = m.head(last_rows(x, b1 - b0))
             for t in range(1, D + 1):
                 x = decode_rows(b0, b1, t)
                 for j in range(nl):
                     x = layer_step(m.layers[j], x, caches[j].view(b0, b1), DECODE,
-                                   b1 - b0, 1, pos=s + t - 1)
+                                   b1 - b0, 1, pos=s + t - 1, pad=pb)
                 out[t][b0:b1] = m.head(x)
         return out
 
@@ -213,7 +258,7 @@ def generate(m: OracleModel, prompt_ids, decode_ids, gbs: int, k: int,
     for j in range(nl):
         for bb in groups[0]:
             xs[bb] = layer_step(m.layers[j], xs[bb], caches[j].view(*bb), PREFILL,
-                                bb[1] - bb[0], s)
+                                bb[1] - bb[0], s, pad=pad[bb[0]:bb[1]])
     for (b0, b1) in groups[0]:
         out[0][b0:b1] = m.head(last_rows(xs[(b0, b1)], b1 - b0))
     for t in range(1, D + 1):
@@ -221,7 +266,7 @@ def generate(m: OracleModel, prompt_ids, decode_ids, gbs: int, k: int,
         for j in range(nl):
             for bb in groups[t]:
                 xs[bb] = layer_step(m.layers[j], xs[bb], caches[j].view(*bb), DECODE,
-                                    bb[1] - bb[0], 1, pos=s + t - 1)
+                                    bb[1] - bb[0], 1, pos=s + t - 1, pad=pad[bb[0]:bb[1]])
         for (b0, b1) in groups[t]:
             out[t][b0:b1] = m.head(xs[(b0, b1)])
     return out

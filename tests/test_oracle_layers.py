@@ -284,3 +284,103 @@ def test_prefill_store_matches_row_quantisation():
                 assert np.array_equal(c.v_codes[b, h, t], vc[0])
                 assert np.array_equal(c.k_meta[b, h, t], km[0])
                 assert np.array_equal(c.v_meta[b, h, t], vm[0])
+
+
+# ------------------------------------------------------------------ left padding
+
+def _prefill_ref_padded(qkv, B, s, H, d, pad):
+    """fp64 softmax with the causal mask and keys before pad[b] masked; rows
+    in padding slots are zero."""
+    h1 = H * d
+    q = qkv[:, :h1].astype(np.float64).reshape(B, s, H, d)
+    k = qkv[:, h1:2 * h1].astype(np.float64).reshape(B, s, H, d)
+    v = qkv[:, 2 * h1:].astype(np.float64).reshape(B, s, H, d)
+    o = np.zeros((B, s, H, d))
+    for b in range(B):
+        p0 = pad[b]
+        sc = np.einsum("ihc,jhc->hij", q[b, p0:], k[b, p0:]) / np.sqrt(d)
+        n = s - p0
+        sc = np.where(np.tril(np.ones((n, n), bool)), sc, -np.inf)
+        o[b, p0:] = np.einsum("hij,jhc->ihc", softmax(sc, axis=-1), v[b, p0:])
+    return o.reshape(B * s, h1)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_padded_against_scipy_softmax(d):
+    rng = np.random.default_rng(31 + d)
+    B, s, H = 3, 9, 2
+    pad = np.array([0, 4, 8], np.int32)
+    qkv = _qkv(rng, B, s, H, d)
+    out = oracle.prefill_attn(qkv, B, s, H, d, pad=pad).astype(np.float64)
+    ref = _prefill_ref_padded(qkv, B, s, H, d, pad)
+    assert np.all(np.abs(out - ref) <= half_ulp(ref) + 1e-5 * (1 + np.abs(ref)))
+    rows = out.reshape(B, s, -1)
+    assert not np.any(rows[1, :4]) and not np.any(rows[2, :8])
+
+
+def test_prefill_padded_equals_unpadded():
+    """Padding never reaches a real token: the rows of a padded prompt equal,
+    bit for bit, the same prompt run alone at its own length, whatever the
+    padding slots hold."""
+    rng = np.random.default_rng(33)
+    B, s, H, d = 2, 11, 2, 64
+    pad = np.array([5, 0], np.int32)
+    qkv = _qkv(rng, B, s, H, d)
+    qkv[:5] = f16(1e3 * rng.standard_normal((5, qkv.shape[1])))   # junk in padding slots
+    out = oracle.prefill_attn(qkv, B, s, H, d, pad=pad)
+    alone = oracle.prefill_attn(qkv[5:s], 1, s - 5, H, d)
+    assert np.array_equal(out[5:s], alone)
+    assert np.array_equal(out[s:], oracle.prefill_attn(qkv[s:], 1, s, H, d))
+
+
+def test_decode_padded_against_scipy_softmax():
+    rng = np.random.default_rng(34)
+    B, H, d, L = 3, 2, 128, 10
+    pad = np.array([0, 3, 9], np.int32)
+    c = _filled_cache(rng, B, H, d, L + 1, L - 1)
+    qkv = _qkv(rng, B, 1, H, d)
+    out = oracle.decode_attn_g4(qkv, c, L - 1, append=True, pad=pad).astype(np.float64)
+    for b in range(B):
+        sub = oracle.KVCache(1, H, d, L)
+        p0 = pad[b]
+        n = L - p0
+        sub.k_codes[0, :, :n], sub.k_meta[0, :, :n] = c.k_codes[b, :, p0:L], c.k_meta[b, :, p0:L]
+        sub.v_codes[0, :, :n], sub.v_meta[0, :, :n] = c.v_codes[b, :, p0:L], c.v_meta[b, :, p0:L]
+        ref = _decode_ref(qkv[b:b + 1], sub, n - 1)
+        assert np.all(np.abs(out[b] - ref[0]) <= half_ulp(ref[0]) + 1e-5 * (1 + np.abs(ref[0])))
+
+
+def test_decode_padded_equals_unpadded():
+    """Attending slots pad..pos equals, bit for bit, attending the same rows
+    moved to slots 0..pos-pad."""
+    rng = np.random.default_rng(35)
+    B, H, d, L, p0 = 1, 2, 64, 13, 6
+    c = _filled_cache(rng, B, H, d, L, L - 1)
+    qkv = _qkv(rng, B, 1, H, d)
+    a = oracle.decode_attn_g4(qkv, c, L - 1, append=True, pad=np.array([p0], np.int32))
+    c2 = oracle.KVCache(B, H, d, L)
+    for src, dst in ((c.k_codes, c2.k_codes), (c.k_meta, c2.k_meta),
+                     (c.v_codes, c2.v_codes), (c.v_meta, c2.v_meta)):
+        dst[:, :, :L - p0] = src[:, :, p0:L]
+    b = oracle.decode_attn_g4(qkv, c2, L - 1 - p0, append=False)
+    assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------ greedy choice
+
+def test_argmax_matches_numpy_first_occurrence():
+    rng = np.random.default_rng(36)
+    x = rng.standard_normal((7, 1001)).astype(np.float32)
+    assert np.array_equal(oracle.argmax(x), np.argmax(x, axis=1))
+    # rounded to few values: many ties, the lowest index wins
+    y = np.round(rng.standard_normal((9, 333)), 0).astype(np.float32)
+    assert np.array_equal(oracle.argmax(y), np.argmax(y, axis=1))
+
+
+def test_argmax_ties_pick_lowest_index():
+    x = np.zeros((3, 10), np.float32)
+    x[0, [2, 7]] = 5.0
+    x[1, :] = -1.0
+    x[2, [9]] = 1.0
+    x[2, [4]] = 1.0
+    assert list(oracle.argmax(x)) == [2, 0, 4]

@@ -15,7 +15,8 @@ import torch
 
 import oracle
 import synth
-from oracle.model import DECODE, PREFILL, OracleModel, generate, layer_step, quantize_layer
+from oracle.model import (DECODE, PREFILL, OracleModel, generate, generate_greedy,
+                          layer_step, quantize_layer)
 
 GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_examples.json")))
 
@@ -166,3 +167,44 @@ def test_decode_step_extends_prefill():
     yp = layer_step(L, x, c2, PREFILL, 1, s + 1)[-1:].astype(np.float64)
     rel = np.linalg.norm(yd - yp) / np.linalg.norm(yp)
     assert rel < 2e-2
+
+
+# ------------------------------------------------------------------ padding and greedy
+
+@pytest.mark.parametrize("order", ["row", "zigzag", "block"])
+def test_padded_prompt_equals_unpadded_run(order):
+    """Left padding reaches no real token: a prompt padded inside a block of
+    longer prompts gives, bit for bit, the logits (teacher-forced) and the
+    tokens (greedy) of the same prompt run alone at its own length."""
+    m = _tiny_model(seed=7)
+    g = synth.generator(8)
+    gbs, k, s, D = 2, 2, 9, 3
+    pad = np.array([0, 4, 8, 1], np.int32)
+    prompt = synth.token_ids((gbs * k, s), 300, g).numpy()
+    dec = synth.token_ids((gbs * k, D), 300, g).numpy()
+    full = generate(m, prompt, dec, gbs, k, order=order, pad=pad)
+    toks, glog = generate_greedy(m, prompt, D + 1, gbs, k, order=order, pad=pad)
+    for b in range(gbs * k):
+        p0 = pad[b]
+        one = generate(m, prompt[b:b + 1, p0:], dec[b:b + 1], 1, 1, order="block")
+        for x, y in zip(full, one):
+            assert np.array_equal(x[b:b + 1], y)
+        t1, _ = generate_greedy(m, prompt[b:b + 1, p0:], D + 1, 1, 1, order="block")
+        assert np.array_equal(toks[b:b + 1], t1)
+
+
+def test_greedy_feeds_back_its_argmax():
+    """Greedy tokens are the argmax of each step's logits, and feeding them
+    back teacher-forced reproduces the same logits."""
+    m = _tiny_model(seed=9)
+    g = synth.generator(10)
+    gbs, k, s, n = 3, 2, 6, 4
+    prompt = synth.token_ids((gbs * k, s), 300, g).numpy()
+    pad = np.array([0, 2, 5, 0, 3, 1], np.int32)
+    toks, logits = generate_greedy(m, prompt, n, gbs, k, order="zigzag", pad=pad)
+    assert toks.shape == (gbs * k, n)
+    for t in range(n):
+        assert np.array_equal(toks[:, t], np.argmax(logits[t], axis=1))
+    tf = generate(m, prompt, toks[:, :n - 1], gbs, k, order="block", pad=pad)
+    for x, y in zip(logits, tf):
+        assert np.array_equal(x, y)
