@@ -265,7 +265,7 @@ const char* fg_status_str(fg_status s) {
 
 const char* fg_last_error(void) { return g_err; }
 
-int32_t fg_version(void) { return (1 << 16) | 0; }
+int32_t fg_version(void) { return (2 << 16) | 0; }
 
 fg_status fg_check(fg_stream stream) {
     cudaError_t e = cudaStreamSynchronize(S(stream));
@@ -392,9 +392,9 @@ fg_status fg_layernorm(const fg_f16* x, int64_t rows, int64_t cols, int64_t x_ld
     return fg::launch_layernorm(H(x), rows, cols, x_ld, H(gamma), H(beta), eps, Hm(y), S(stream));
 }
 
-fg_status fg_embed(const int32_t* ids, int64_t ntok, int32_t T, int32_t pos0, const fg_f16* e_tok,
-                   int64_t vocab, const fg_f16* e_pos, int64_t npos, int32_t h1, fg_f16* y,
-                   fg_stream stream) {
+fg_status fg_embed(const int32_t* ids, int64_t ntok, int32_t T, int32_t pos0, const int32_t* pad,
+                   const fg_f16* e_tok, int64_t vocab, const fg_f16* e_pos, int64_t npos,
+                   int32_t h1, fg_f16* y, fg_stream stream) {
     FG_REQUIRE(ids && e_tok && e_pos && y, FG_ERR_NULL, "embed: null pointer");
     FG_REQUIRE(ntok >= 0 && T > 0 && ntok % T == 0 && pos0 >= 0 && h1 > 0 && h1 % 8 == 0 &&
                    vocab > 0 && pos0 + T <= npos,
@@ -402,7 +402,18 @@ fg_status fg_embed(const int32_t* ids, int64_t ntok, int32_t T, int32_t pos0, co
                (long long)ntok, T, pos0, (long long)npos);
     FG_REQUIRE(fg::aligned16(e_tok) && fg::aligned16(e_pos) && fg::aligned16(y), FG_ERR_ALIGN,
                "embed: tables and y must be 16-byte aligned");
-    return fg::launch_embed(ids, ntok, T, pos0, H(e_tok), H(e_pos), h1, Hm(y), S(stream));
+    return fg::launch_embed(ids, ntok, T, pos0, pad, H(e_tok), H(e_pos), h1, Hm(y), S(stream));
+}
+
+fg_status fg_argmax(const float* logits, int64_t B, int64_t V, int32_t* out, fg_stream stream) {
+    FG_REQUIRE(B >= 0 && V > 0 && V < (1LL << 31) && B < (1LL << 31), FG_ERR_SHAPE,
+               "argmax: bad sizes (B %lld, V %lld)", (long long)B, (long long)V);
+    if (B == 0) return FG_OK;
+    FG_REQUIRE(logits && out, FG_ERR_NULL, "argmax: null pointer");
+    FG_REQUIRE((reinterpret_cast<uintptr_t>(logits) & 3u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(out) & 3u) == 0,
+               FG_ERR_ALIGN, "argmax: pointers must be 4-byte aligned");
+    return fg::launch_argmax(logits, B, V, out, S(stream));
 }
 
 fg_status fg_kv_append_g4(const fg_f16* qkv, int64_t qkv_ld, const fg_kv4* cache, int32_t pos,
@@ -421,7 +432,8 @@ fg_status fg_kv_append_g4(const fg_f16* qkv, int64_t qkv_ld, const fg_kv4* cache
 }
 
 fg_status fg_decode_attn_g4(const fg_f16* qkv, int64_t qkv_ld, const fg_kv4* cache, int32_t pos,
-                            int32_t fuse_append, fg_f16* out, fg_stream stream) {
+                            const int32_t* pad, int32_t fuse_append, fg_f16* out,
+                            fg_stream stream) {
     fg_status s = check_kv(cache, "decode_attn_g4");
     if (s != FG_OK) return s;
     FG_REQUIRE(qkv && out, FG_ERR_NULL, "decode_attn_g4: null qkv or out");
@@ -433,11 +445,15 @@ fg_status fg_decode_attn_g4(const fg_f16* qkv, int64_t qkv_ld, const fg_kv4* cac
     FG_REQUIRE(cache->cap <= 50000, FG_ERR_UNSUPPORTED, "decode_attn_g4: cap %d > 50000", cache->cap);
     FG_REQUIRE(fg::aligned16(qkv) && fg::aligned16(out), FG_ERR_ALIGN,
                "decode_attn_g4: qkv and out must be 16-byte aligned");
-    return fg::launch_decode_attn(H(qkv), qkv_ld, cache, pos, fuse_append, Hm(out), S(stream));
+    FG_REQUIRE((reinterpret_cast<uintptr_t>(pad) & 3u) == 0, FG_ERR_ALIGN,
+               "decode_attn_g4: pad must be 4-byte aligned");
+    return fg::launch_decode_attn(H(qkv), qkv_ld, cache, pos, pad, fuse_append, Hm(out),
+                                  S(stream));
 }
 
 fg_status fg_prefill_attn(const fg_f16* qkv, int32_t B, int32_t s_len, int32_t Hh, int32_t d,
-                          const fg_kv4* cache, fg_f16* out, fg_stream stream) {
+                          const int32_t* pad, const fg_kv4* cache, fg_f16* out,
+                          fg_stream stream) {
     FG_REQUIRE(qkv && out, FG_ERR_NULL, "prefill_attn: null qkv or out");
     FG_REQUIRE(B >= 0 && s_len >= 0 && Hh > 0, FG_ERR_SHAPE, "prefill_attn: bad B/s/H");
     FG_REQUIRE(d == 64 || d == 128, FG_ERR_UNSUPPORTED, "prefill_attn: head dim %d not in {64,128}", d);
@@ -449,7 +465,9 @@ fg_status fg_prefill_attn(const fg_f16* qkv, int32_t B, int32_t s_len, int32_t H
         FG_REQUIRE(cache->B == B && cache->H == Hh && cache->d == d && s_len <= cache->cap,
                    FG_ERR_SHAPE, "prefill_attn: cache shape does not match");
     }
-    fg_status s = fg::launch_prefill_attn(H(qkv), B, s_len, Hh, d, Hm(out), S(stream));
+    FG_REQUIRE((reinterpret_cast<uintptr_t>(pad) & 3u) == 0, FG_ERR_ALIGN,
+               "prefill_attn: pad must be 4-byte aligned");
+    fg_status s = fg::launch_prefill_attn(H(qkv), B, s_len, Hh, d, pad, Hm(out), S(stream));
     if (s != FG_OK || !cache) return s;
     return fg::launch_kv_store(H(qkv), 3LL * Hh * d, B, s_len, Hh, d, cache, 0, S(stream));
 }
@@ -464,13 +482,15 @@ size_t fg_layer_workspace_bytes(const fg_layer* w, int32_t phase, int32_t bls, i
 }
 
 fg_status fg_layer_step(const fg_layer* w, const fg_kv4* cache, const fg_f16* x_in, fg_f16* x_out,
-                        int32_t phase, int32_t T, int32_t pos, fg_policy p, void* workspace,
-                        size_t ws_bytes, fg_stream stream) {
+                        int32_t phase, int32_t T, int32_t pos, const int32_t* pad, fg_policy p,
+                        void* workspace, size_t ws_bytes, fg_stream stream) {
     fg_status s = check_layer(w);
     if (s != FG_OK) return s;
     if ((s = check_kv(cache, "layer_step")) != FG_OK) return s;
     FG_REQUIRE(x_in && x_out, FG_ERR_NULL, "layer_step: null x_in or x_out");
     FG_REQUIRE(x_in != x_out, FG_ERR_SHAPE, "layer_step: x_in and x_out may not alias");
+    FG_REQUIRE((reinterpret_cast<uintptr_t>(pad) & 3u) == 0, FG_ERR_ALIGN,
+               "layer_step: pad must be 4-byte aligned");
     FG_REQUIRE(fg::aligned16(x_in) && fg::aligned16(x_out), FG_ERR_ALIGN,
                "layer_step: x_in and x_out must be 16-byte aligned");
     FG_REQUIRE(p.gbs > 0 && p.k > 0 && p.order >= 0 && p.order <= 2, FG_ERR_SHAPE,
@@ -507,6 +527,7 @@ fg_status fg_layer_step(const fg_layer* w, const fg_kv4* cache, const fg_f16* x_
         const int32_t b0 = bi * nb;
         const int64_t r0 = static_cast<int64_t>(b0) * T, nr = static_cast<int64_t>(nb) * T;
         const fg_kv4 c = sub_cache(cache, b0, nb);
+        const int32_t* pb = pad ? pad + b0 : nullptr;
         const __half* xin = H(x_in) + r0 * h1;
         __half* xout = Hm(x_out) + r0 * h1;
         __half* a = L.a + r0 * h1;
@@ -523,10 +544,10 @@ fg_status fg_layer_step(const fg_layer* w, const fg_kv4* cache, const fg_f16* x_
         FG_RUN(fg::launch_gemm_g4(a, nr, &w->qkv, H(w->b_qkv), nullptr, FG_ACT_NONE, qkv, L.gemm,
                                   L.gemm_bytes, st, rows));
         if (phase == FG_PHASE_PREFILL) {
-            FG_RUN(fg::launch_prefill_attn(qkv, nb, T, w->H, d, attn, st));
+            FG_RUN(fg::launch_prefill_attn(qkv, nb, T, w->H, d, pb, attn, st));
             FG_RUN(fg::launch_kv_store(qkv, 3 * h1, nb, T, w->H, d, &c, 0, st));
         } else {
-            FG_RUN(fg::launch_decode_attn(qkv, 3 * h1, &c, pos, 1, attn, st));
+            FG_RUN(fg::launch_decode_attn(qkv, 3 * h1, &c, pos, pb, 1, attn, st));
         }
         FG_RUN(fg::launch_gemm_g4(attn, nr, &w->out, H(w->b_out), xin, FG_ACT_NONE, hh, L.gemm,
                                   L.gemm_bytes, st, rows));

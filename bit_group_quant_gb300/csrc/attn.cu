@@ -7,6 +7,11 @@
 // cached rows.  Stored 4-bit tensors are dequantised to FP16 before use
 // (section on compression), so every cached row -- the new one included --
 // is read back through dequantisation.
+//
+// Left padding (prompts of different lengths in one block): sequence b's
+// tokens occupy slots pad[b].. of its rows; every query attends only keys at
+// slots >= pad[b], and prefill queries in padding slots output zeros.  With
+// pad NULL every sequence starts at slot 0.
 #include <math_constants.h>
 
 #include "fg_internal.cuh"
@@ -79,8 +84,8 @@ __device__ __forceinline__ uint32_t ldg32(const uint8_t* p) {
 template <int D>
 __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
     const __half* __restrict__ qkv, int64_t ld, int32_t H, int32_t cap, int32_t pos,
-    int32_t fuse_append, uint8_t* k_codes, uint8_t* v_codes, float* k_meta, float* v_meta,
-    __half* __restrict__ out) {
+    const int32_t* __restrict__ pad, int32_t fuse_append, uint8_t* k_codes, uint8_t* v_codes,
+    float* k_meta, float* v_meta, __half* __restrict__ out) {
     constexpr int G = D / 64;            // groups per head row
     constexpr int RB = D / 2;            // code bytes per row
     constexpr int WPT = D / 32;          // code words per lane per row in pass 1
@@ -93,9 +98,12 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
     __shared__ float part_s[NWARP][2][2];   // per warp, per group: sum p m, sum p'
 
     const int h = blockIdx.x, b = blockIdx.y;
-    const int L = pos + 1;
+    // attended slots p0..pos (a padding count outside [0, pos] is clamped)
+    const int p0 = pad ? min(max(pad[b], 0), pos) : 0;
+    const int L = pos + 1 - p0;
     const int64_t h1 = static_cast<int64_t>(H) * D;
-    const int64_t row0 = (static_cast<int64_t>(b) * H + h) * cap;  // cache row of slot 0
+    const int64_t rowb = (static_cast<int64_t>(b) * H + h) * cap;  // cache row of slot 0
+    const int64_t row0 = rowb + p0;                                 // first attended row
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     float* sc = dsm;
@@ -122,7 +130,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
         float mn, scale;
         const uint32_t packed = quantize8(v, mn, scale);
         if (valid) {
-            const int64_t row = row0 + pos;
+            const int64_t row = rowb + pos;
             uint8_t* cdst = (is_v ? v_codes : k_codes) + row * RB + gi * 32;
             reinterpret_cast<uint32_t*>(cdst)[lane8] = packed;
             if (lane8 == 0) {
@@ -361,8 +369,9 @@ constexpr int kChunkBytes = kCKMax * (kRB128 + kMB128);   // codes, then meta
 
 __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_kernel(
     const __half* __restrict__ qkv, int64_t ld, int32_t H, int32_t cap, int32_t pos,
-    int32_t fuse_append, uint8_t* k_codes, uint8_t* v_codes, float* k_meta, float* v_meta,
-    __half* __restrict__ out, int* status, unsigned long long wait_ns) {
+    const int32_t* __restrict__ pad, int32_t fuse_append, uint8_t* k_codes, uint8_t* v_codes,
+    float* k_meta, float* v_meta, __half* __restrict__ out, int* status,
+    unsigned long long wait_ns) {
     constexpr int D = 128, G = 2, RB = kRB128, WPT = D / 32, NX = 2 * WPT;
     constexpr int NWARP = kDecThreads / 32;
     extern __shared__ __align__(128) uint8_t dyn[];
@@ -374,14 +383,17 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     __shared__ int fail_sh;
 
     const int h = blockIdx.x, b = blockIdx.y;
-    const int L = pos + 1;
+    // attended slots p0..pos (a padding count outside [0, pos] is clamped)
+    const int p0 = pad ? min(max(pad[b], 0), pos) : 0;
+    const int L = pos + 1 - p0;
     // chunks of kCK keys; a remainder of <= 16 keys joins the last full chunk
     int nK = (L + kCK - 1) / kCK;
     if (nK > 1 && L - (nK - 1) * kCK <= 16) --nK;
     const int nseq = 2 * nK;
     auto chunk_n = [&](int c) { return c == nK - 1 ? L - c * kCK : kCK; };
     const int64_t h1 = static_cast<int64_t>(H) * D;
-    const int64_t row0 = (static_cast<int64_t>(b) * H + h) * cap;
+    const int64_t rowb = (static_cast<int64_t>(b) * H + h) * cap;  // cache row of slot 0
+    const int64_t row0 = rowb + p0;                                 // first attended row
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const uint32_t ring = smem_u32(dyn);
@@ -409,7 +421,7 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
         float mn, scale;
         const uint32_t packed = quantize8(v, mn, scale);
         if (valid) {
-            const int64_t row = row0 + pos;
+            const int64_t row = rowb + pos;
             uint8_t* cdst = (is_v ? v_codes : k_codes) + row * RB + gi * 32;
             reinterpret_cast<uint32_t*>(cdst)[lane8] = packed;
             if (lane8 == 0) {
@@ -668,103 +680,6 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     }
 }
 
-// Causal prefill attention over fp16 Q/K/V.  One CTA per (32-query tile,
-// head, sequence); 4 threads per query, each owning D/4 interleaved dims
-// (dim = 4*e + part) so the 4 reads of a key row hit 4 different banks.
-constexpr int kPreQ = 32;
-constexpr int kPreK = 32;
-
-template <int D>
-__global__ void __launch_bounds__(128) prefill_attn_kernel(const __half* __restrict__ qkv,
-                                                           int32_t s, int32_t H,
-                                                           __half* __restrict__ out) {
-    constexpr int DP = D / 4;
-    __shared__ float Ks[kPreK][D];
-    __shared__ float Vs[kPreK][D];
-    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int64_t h1 = static_cast<int64_t>(H) * D, ld = 3 * h1;
-    const int part = threadIdx.x & 3;
-    const int i = qt * kPreQ + (threadIdx.x >> 2);
-    const unsigned gmask = 0xFu << (threadIdx.x & 28);
-    const __half* base = qkv + static_cast<int64_t>(b) * s * ld + static_cast<int64_t>(h) * D;
-    const float scale = __fdiv_rn(1.0f, __fsqrt_rn(static_cast<float>(D)));
-
-    float q[DP], acc[DP];
-    float m = -CUDART_INF_F, l = 0.0f;
-#pragma unroll
-    for (int e = 0; e < DP; ++e) {
-        q[e] = (i < s) ? __half2float(base[static_cast<int64_t>(i) * ld + 4 * e + part]) : 0.0f;
-        acc[e] = 0.0f;
-    }
-    const int last_q = min(s - 1, qt * kPreQ + kPreQ - 1);
-    for (int k0 = 0; k0 <= last_q; k0 += kPreK) {
-        __syncthreads();
-        for (int t = threadIdx.x; t < kPreK * D / 8; t += blockDim.x) {
-            const int jj = t / (D / 8), c = (t % (D / 8)) * 8;
-            const int j = k0 + jj;
-            float kv[8], vv[8];
-            if (j < s) {
-                const uint4 kr = *reinterpret_cast<const uint4*>(base + static_cast<int64_t>(j) * ld + h1 + c);
-                const uint4 vr = *reinterpret_cast<const uint4*>(base + static_cast<int64_t>(j) * ld + 2 * h1 + c);
-                const __half2* kh = reinterpret_cast<const __half2*>(&kr);
-                const __half2* vh = reinterpret_cast<const __half2*>(&vr);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float2 kf = __half22float2(kh[u]);
-                    const float2 vf = __half22float2(vh[u]);
-                    kv[2 * u] = kf.x;
-                    kv[2 * u + 1] = kf.y;
-                    vv[2 * u] = vf.x;
-                    vv[2 * u + 1] = vf.y;
-                }
-            } else {
-#pragma unroll
-                for (int u = 0; u < 8; ++u) kv[u] = vv[u] = 0.0f;
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                Ks[jj][c + u] = kv[u];
-                Vs[jj][c + u] = vv[u];
-            }
-        }
-        __syncthreads();
-        if (i < s) {
-            float sc[kPreK];
-            float tmax = -CUDART_INF_F;
-#pragma unroll
-            for (int jj = 0; jj < kPreK; ++jj) {
-                float dot = 0.0f;
-#pragma unroll
-                for (int e = 0; e < DP; ++e) dot += q[e] * Ks[jj][4 * e + part];
-                dot += __shfl_xor_sync(gmask, dot, 1);
-                dot += __shfl_xor_sync(gmask, dot, 2);
-                const bool ok = (k0 + jj) <= i;
-                sc[jj] = ok ? dot * scale : -CUDART_INF_F;
-                tmax = fmaxf(tmax, sc[jj]);
-            }
-            const float mnew = fmaxf(m, tmax);
-            const float corr = expf(m - mnew);
-            l *= corr;
-#pragma unroll
-            for (int e = 0; e < DP; ++e) acc[e] *= corr;
-#pragma unroll
-            for (int jj = 0; jj < kPreK; ++jj) {
-                const float p = expf(sc[jj] - mnew);
-                l += p;
-#pragma unroll
-                for (int e = 0; e < DP; ++e) acc[e] += p * Vs[jj][4 * e + part];
-            }
-            m = mnew;
-        }
-    }
-    if (i < s) {
-        __half* o = out + (static_cast<int64_t>(b) * s + i) * h1 + static_cast<int64_t>(h) * D;
-        const float inv = 1.0f / l;
-#pragma unroll
-        for (int e = 0; e < DP; ++e) o[4 * e + part] = __float2half_rn(acc[e] * inv);
-    }
-}
-
 // Causal prefill attention on the tensor cores (flash-attention forward):
 // one CTA of 4 warps per (64-query block, head, sequence), 16 queries per
 // warp; 64-key tiles of K and V double-buffered in shared memory by cp.async
@@ -772,7 +687,11 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const __half* __restr
 // S = Q K^T and O += P V on mma.sync m16n8k16 (fp16 in, fp32 accumulate) with
 // an online softmax in fp32 (P enters the second product as fp16).  Key tiles
 // beyond the block's last query are skipped; the diagonal tile is masked.
-// Query blocks are visited heaviest first.
+// Query blocks are visited heaviest first.  A left-padded sequence is
+// computed as its real part alone: query and key tiles start at its first
+// real slot p0 (Q/K/V and output rows shifted by p0), so every real row is
+// bit-identical to the same prompt run unpadded; block qb also zeroes the
+// padding rows [64 qb, 64 qb + 64) below p0.
 constexpr int kFaM = 64;   // queries per CTA
 constexpr int kFaN = 64;   // keys per tile
 
@@ -800,22 +719,37 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 
 template <int D>
 __global__ void __launch_bounds__(128) prefill_attn_fa_kernel(const __half* __restrict__ qkv,
-                                                              int32_t s, int32_t H,
-                                                              __half* __restrict__ out) {
+                                                              int32_t s_all, int32_t H,
+                                                              const int32_t* __restrict__ pad,
+                                                              __half* __restrict__ out_all) {
     constexpr int CH = D / 8;                 // 16-byte chunks per row
     constexpr int TB = kFaN * D * 2;          // bytes of one K or V tile
     constexpr int KS = D / 16;                // k-steps of Q K^T
     constexpr int NT = D / 8;                 // n-tiles of the output
     extern __shared__ __align__(128) uint8_t fsm[];
     const uint32_t sQ = smem_u32(fsm), sK = sQ + kFaM * D * 2, sV = sK + 2 * TB;
-    const int nqb = (s + kFaM - 1) / kFaM;
+    const int nqb = (s_all + kFaM - 1) / kFaM;
     const int qb = nqb - 1 - static_cast<int>(blockIdx.x);   // heaviest first
     const int h = blockIdx.y, b = blockIdx.z;
     const int64_t h1 = static_cast<int64_t>(H) * D, ld = 3 * h1;
-    const __half* base = qkv + static_cast<int64_t>(b) * s * ld + static_cast<int64_t>(h) * D;
+    // first real slot (a padding count outside [0, s_all) is clamped)
+    const int p0 = pad ? min(max(pad[b], 0), s_all - 1) : 0;
+    // output row r of the sequence (slot r), this head
+    auto out_row = [&](int r) {
+        return out_all + (static_cast<int64_t>(b) * s_all + r) * h1 + static_cast<int64_t>(h) * D;
+    };
+    for (int i = threadIdx.x; i < kFaM * CH; i += 128) {   // padding rows of this block: zeros
+        const int row = qb * kFaM + i / CH;
+        if (row < p0) *reinterpret_cast<uint4*>(out_row(row) + (i % CH) * 8) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    // the real part: s rows starting at slot p0
+    const int s = s_all - p0;
+    const int q0 = qb * kFaM;
+    if (q0 >= s) return;
+    const __half* base = qkv + (static_cast<int64_t>(b) * s_all + p0) * ld +
+                         static_cast<int64_t>(h) * D;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int q0 = qb * kFaM;
     // swizzled byte offset of (row, 16-byte chunk) inside a [rows][D] fp16 tile
     auto swz = [](int r, int c) { return static_cast<uint32_t>(r * D * 2 + ((c ^ (r & 7)) << 4)); };
     // one [64][D] tile of rows r0.. of block `part` (0 q, 1 k, 2 v); rows past s read as zeros
@@ -843,9 +777,10 @@ __global__ void __launch_bounds__(128) prefill_attn_fa_kernel(const __half* __re
     const int qr0 = warp * 16;   // this warp's rows in the block
 
     for (int j = 0; j < ntiles; ++j) {
+        const int buf = j & 1;
         if (j + 1 < ntiles) {   // prefetch the next tile into the other buffer
-            load_tile(sK + ((j + 1) & 1) * TB, 1, (j + 1) * kFaN);
-            load_tile(sV + ((j + 1) & 1) * TB, 2, (j + 1) * kFaN);
+            load_tile(sK + (buf ^ 1) * TB, 1, (j + 1) * kFaN);
+            load_tile(sV + (buf ^ 1) * TB, 2, (j + 1) * kFaN);
         }
         cp_async_commit();
         cp_async_wait<1>();
@@ -856,7 +791,7 @@ __global__ void __launch_bounds__(128) prefill_attn_fa_kernel(const __half* __re
                 ldsm_x4(sQ + swz(qr0 + (lane & 15), 2 * kk + (lane >> 4)), qf[kk][0], qf[kk][1],
                         qf[kk][2], qf[kk][3]);
         }
-        const uint32_t kb = sK + (j & 1) * TB, vb = sV + (j & 1) * TB;
+        const uint32_t kb = sK + buf * TB, vb = sV + buf * TB;
         // ---- S = Q K^T for 64 keys: 8 n-tiles
         float sacc[8][4];
 #pragma unroll
@@ -937,7 +872,7 @@ __global__ void __launch_bounds__(128) prefill_attn_fa_kernel(const __half* __re
         const int qi = q0 + qr0 + g + 8 * r;
         if (qi < s) {
             const float inv = 1.0f / lsum;
-            __half* orow = out + (static_cast<int64_t>(b) * s + qi) * h1 + static_cast<int64_t>(h) * D;
+            __half* orow = out_row(p0 + qi);
 #pragma unroll
             for (int n = 0; n < NT; ++n)
                 *reinterpret_cast<uint32_t*>(orow + 8 * n + 2 * t) =
@@ -948,7 +883,7 @@ __global__ void __launch_bounds__(128) prefill_attn_fa_kernel(const __half* __re
 
 template <int D>
 fg_status launch_decode_t(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
-                          int32_t fuse_append, __half* out, cudaStream_t st) {
+                          const int32_t* pad, int32_t fuse_append, __half* out, cudaStream_t st) {
     const int L = pos + 1;
     const size_t smem = sizeof(float) * ((L + 3) & ~3);
     auto kern = decode_attn_kernel<D>;
@@ -964,13 +899,14 @@ fg_status launch_decode_t(const __half* qkv, int64_t ld, const fg_kv4* c, int32_
     const double bh = static_cast<double>(c->B) * c->H;
     fg::TraceScope ts(FG_TRACE_ATTN_DECODE, st, 4.0 * bh * L * D,
                       bh * (2.0 * L * row + (fuse_append ? 2.0 * row : 0.0) + 3.0 * D * 2 + D * 2));
-    kern<<<grid, kDecThreads, smem, st>>>(qkv, ld, c->H, c->cap, pos, fuse_append, c->k_codes,
-                                          c->v_codes, c->k_meta, c->v_meta, out);
+    kern<<<grid, kDecThreads, smem, st>>>(qkv, ld, c->H, c->cap, pos, pad, fuse_append,
+                                          c->k_codes, c->v_codes, c->k_meta, c->v_meta, out);
     return fg::cuda_error(cudaGetLastError(), "decode_attn launch");
 }
 
 fg_status launch_decode_staged(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
-                               int32_t fuse_append, __half* out, cudaStream_t st) {
+                               const int32_t* pad, int32_t fuse_append, __half* out,
+                               cudaStream_t st) {
     constexpr int D = 128;
     const int L = pos + 1;
     const size_t smem = static_cast<size_t>(kNB) * kChunkBytes + sizeof(float) * ((L + 3) & ~3);
@@ -983,8 +919,8 @@ fg_status launch_decode_staged(const __half* qkv, int64_t ld, const fg_kv4* c, i
     const double bh = static_cast<double>(c->B) * c->H;
     fg::TraceScope ts(FG_TRACE_ATTN_DECODE, st, 4.0 * bh * L * D,
                       bh * (2.0 * L * row + (fuse_append ? 2.0 * row : 0.0) + 3.0 * D * 2 + D * 2));
-    kern<<<grid, kDecThreads, smem, st>>>(qkv, ld, c->H, c->cap, pos, fuse_append, c->k_codes,
-                                          c->v_codes, c->k_meta, c->v_meta, out,
+    kern<<<grid, kDecThreads, smem, st>>>(qkv, ld, c->H, c->cap, pos, pad, fuse_append,
+                                          c->k_codes, c->v_codes, c->k_meta, c->v_meta, out,
                                           fg::device_status_ptr(), fg::wait_limit_ns());
     return fg::cuda_error(cudaGetLastError(), "decode_attn launch");
 }
@@ -994,14 +930,15 @@ fg_status launch_decode_staged(const __half* qkv, int64_t ld, const fg_kv4* c, i
 namespace fg {
 
 fg_status launch_decode_attn(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
-                             int32_t fuse_append, __half* out, cudaStream_t st) {
+                             const int32_t* pad, int32_t fuse_append, __half* out,
+                             cudaStream_t st) {
     if (c->B == 0) return FG_OK;
-    if (c->d == 64) return launch_decode_t<64>(qkv, ld, c, pos, fuse_append, out, st);
-    return launch_decode_staged(qkv, ld, c, pos, fuse_append, out, st);
+    if (c->d == 64) return launch_decode_t<64>(qkv, ld, c, pos, pad, fuse_append, out, st);
+    return launch_decode_staged(qkv, ld, c, pos, pad, fuse_append, out, st);
 }
 
 fg_status launch_prefill_attn(const __half* qkv, int32_t B, int32_t s, int32_t H, int32_t d,
-                              __half* out, cudaStream_t st) {
+                              const int32_t* pad, __half* out, cudaStream_t st) {
     if (B == 0 || s == 0) return FG_OK;
     dim3 grid(static_cast<unsigned>(cdiv(s, kFaM)), H, B);
     const double bh = static_cast<double>(B) * H;
@@ -1013,13 +950,13 @@ fg_status launch_prefill_attn(const __half* qkv, int32_t B, int32_t s, int32_t H
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return cuda_error(e, "prefill_attn smem attribute");
-        kern<<<grid, 128, smem, st>>>(qkv, s, H, out);
+        kern<<<grid, 128, smem, st>>>(qkv, s, H, pad, out);
     } else {
         auto kern = prefill_attn_fa_kernel<128>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return cuda_error(e, "prefill_attn smem attribute");
-        kern<<<grid, 128, smem, st>>>(qkv, s, H, out);
+        kern<<<grid, 128, smem, st>>>(qkv, s, H, pad, out);
     }
     return cuda_error(cudaGetLastError(), "prefill_attn launch");
 }

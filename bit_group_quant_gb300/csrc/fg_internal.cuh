@@ -56,12 +56,14 @@ fg_status launch_layernorm(const __half* x, int64_t rows, int64_t cols, int64_t 
                            const __half* g, const __half* b, float eps, __half* y,
                            cudaStream_t st);
 fg_status launch_embed(const int32_t* ids, int64_t ntok, int32_t T, int32_t pos0,
-                       const __half* e_tok, const __half* e_pos, int32_t h1, __half* y,
-                       cudaStream_t st);
+                       const int32_t* pad, const __half* e_tok, const __half* e_pos, int32_t h1,
+                       __half* y, cudaStream_t st);
+fg_status launch_argmax(const float* logits, int64_t B, int64_t V, int32_t* out, cudaStream_t st);
 fg_status launch_decode_attn(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
-                             int32_t fuse_append, __half* out, cudaStream_t st);
+                             const int32_t* pad, int32_t fuse_append, __half* out,
+                             cudaStream_t st);
 fg_status launch_prefill_attn(const __half* qkv, int32_t B, int32_t s, int32_t H, int32_t d,
-                              __half* out, cudaStream_t st);
+                              const int32_t* pad, __half* out, cudaStream_t st);
 
 struct GemmPlan {
     int nt;          // activation rows per tile (MMA N), multiple of 16, <= 256

@@ -1,6 +1,8 @@
-// small.cu -- LayerNorm and token + position embedding (the OPT layer's
-// pre-LN normalisations and the model input).  Both are bandwidth-trivial
-// next to the projections; one CTA per row keeps the row in registers.
+// small.cu -- LayerNorm, token + position embedding and the greedy argmax
+// (the OPT layer's pre-LN normalisations, the model input and the choice of
+// the next token).  All are bandwidth-trivial next to the projections.
+#include <math_constants.h>
+
 #include "fg_internal.cuh"
 
 namespace {
@@ -90,9 +92,12 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const __half* __r
     }
 }
 
-// y[r] = e_tok[ids[r]] + e_pos[pos0 + r % T]  (fp32 add, one rounding).
+// y[r] = e_tok[ids[r]] + e_pos[p]  (fp32 add, one rounding), with
+// p = max(pos0 + r % T - pad[r / T], 0): the position counted from the
+// sequence's first real slot under left padding (pad NULL: no padding).
 __global__ void __launch_bounds__(256) embed_kernel(const int32_t* __restrict__ ids, int64_t ntok,
                                                     int32_t T, int32_t pos0,
+                                                    const int32_t* __restrict__ pad,
                                                     const __half* __restrict__ e_tok,
                                                     const __half* __restrict__ e_pos, int32_t h1,
                                                     __half* __restrict__ y) {
@@ -102,7 +107,8 @@ __global__ void __launch_bounds__(256) embed_kernel(const int32_t* __restrict__ 
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t r = i / nvec, c = i % nvec;
         const int64_t id = ids[r];
-        const int64_t p = pos0 + r % T;
+        const int64_t p0 = pad ? max(pad[r / T], 0) : 0;
+        const int64_t p = max(pos0 + r % T - p0, static_cast<int64_t>(0));
         const uint4 a = reinterpret_cast<const uint4*>(e_tok + id * h1)[c];
         const uint4 bb = reinterpret_cast<const uint4*>(e_pos + p * h1)[c];
         const __half2* ah = reinterpret_cast<const __half2*>(&a);
@@ -117,6 +123,53 @@ __global__ void __launch_bounds__(256) embed_kernel(const int32_t* __restrict__ 
                                    __float2half_rn(__fadd_rn(af.y, bf.y)));
         }
         reinterpret_cast<uint4*>(y + r * h1)[c] = out;
+    }
+}
+
+// Greedy choice per row of fp32 logits: the index of the largest value, the
+// lowest such index among equal values (so the result does not depend on
+// the reduction order).  One CTA per row.
+constexpr int kArgThreads = 512;
+
+struct ValIdx {
+    float v;
+    int32_t i;
+};
+__device__ __forceinline__ ValIdx better(ValIdx a, ValIdx b) {
+    return (b.v > a.v || (b.v == a.v && b.i < a.i)) ? b : a;
+}
+
+__global__ void __launch_bounds__(kArgThreads) argmax_kernel(const float* __restrict__ logits,
+                                                             int64_t V, int32_t* __restrict__ out) {
+    __shared__ ValIdx red[kArgThreads / 32];
+    const float* row = logits + static_cast<int64_t>(blockIdx.x) * V;
+    ValIdx best{-CUDART_INF_F, 0x7fffffff};
+    // 4 independent loads in flight per thread; indices rise within a thread
+    int64_t j = threadIdx.x;
+    for (; j + 3 * kArgThreads < V; j += 4 * kArgThreads) {
+        const float a = row[j], b = row[j + kArgThreads], c = row[j + 2 * kArgThreads],
+                    d = row[j + 3 * kArgThreads];
+        best = better(best, ValIdx{a, static_cast<int32_t>(j)});
+        best = better(best, ValIdx{b, static_cast<int32_t>(j + kArgThreads)});
+        best = better(best, ValIdx{c, static_cast<int32_t>(j + 2 * kArgThreads)});
+        best = better(best, ValIdx{d, static_cast<int32_t>(j + 3 * kArgThreads)});
+    }
+    for (; j < V; j += kArgThreads) best = better(best, ValIdx{row[j], static_cast<int32_t>(j)});
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const ValIdx other{__shfl_xor_sync(0xffffffffu, best.v, o),
+                           __shfl_xor_sync(0xffffffffu, best.i, o)};
+        best = better(best, other);
+    }
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) red[w] = best;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        ValIdx r = red[0];
+#pragma unroll
+        for (int i = 1; i < kArgThreads / 32; ++i) r = better(r, red[i]);
+        // a row of -inf only (never for finite logits) still yields index 0
+        out[blockIdx.x] = r.i == 0x7fffffff ? 0 : r.i;
     }
 }
 
@@ -137,15 +190,22 @@ fg_status launch_layernorm(const __half* x, int64_t rows, int64_t cols, int64_t 
 }
 
 fg_status launch_embed(const int32_t* ids, int64_t ntok, int32_t T, int32_t pos0,
-                       const __half* e_tok, const __half* e_pos, int32_t h1, __half* y,
-                       cudaStream_t st) {
+                       const int32_t* pad, const __half* e_tok, const __half* e_pos, int32_t h1,
+                       __half* y, cudaStream_t st) {
     if (ntok == 0) return FG_OK;
     int64_t blocks = cdiv(ntok * (h1 / 8), 256);
     if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
     TraceScope ts(FG_TRACE_OTHER, st, 0.0, ntok * h1 * 6.0);
-    embed_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(ids, ntok, T, pos0, e_tok, e_pos,
-                                                                h1, y);
+    embed_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(ids, ntok, T, pos0, pad, e_tok,
+                                                                e_pos, h1, y);
     return cuda_error(cudaGetLastError(), "embed launch");
+}
+
+fg_status launch_argmax(const float* logits, int64_t B, int64_t V, int32_t* out, cudaStream_t st) {
+    if (B == 0) return FG_OK;
+    TraceScope ts(FG_TRACE_OTHER, st, 0.0, B * V * 4.0 + B * 4.0);
+    argmax_kernel<<<static_cast<unsigned>(B), kArgThreads, 0, st>>>(logits, V, out);
+    return cuda_error(cudaGetLastError(), "argmax launch");
 }
 
 }  // namespace fg

@@ -29,6 +29,7 @@ EXPORTS = (
     "fg_gemm_f16_f32out", "fg_layernorm", "fg_embed", "fg_kv_append_g4",
     "fg_decode_attn_g4", "fg_prefill_attn", "fg_layer_workspace_bytes", "fg_layer_step",
     "fg_debug_set", "fg_trace_begin", "fg_trace_end", "fg_dequant_gemm_g4_noalloc",
+    "fg_argmax",
 )
 
 
@@ -102,13 +103,14 @@ def load(path: str = LIB_PATH):
             "fg_gemm_f16_f32out": ([P, I64, P, I64, I64, P, P], st),
             "fg_dequant_gemm_g4_noalloc": ([P, I64, ctypes.POINTER(c_q4), P, P, I32, P, P], st),
             "fg_layernorm": ([P, I64, I64, I64, P, P, F, P, P], st),
-            "fg_embed": ([P, I64, I32, I32, P, I64, P, I64, I32, P, P], st),
+            "fg_embed": ([P, I64, I32, I32, P, P, I64, P, I64, I32, P, P], st),
+            "fg_argmax": ([P, I64, I64, P, P], st),
             "fg_kv_append_g4": ([P, I64, ctypes.POINTER(c_kv4), I32, P], st),
-            "fg_decode_attn_g4": ([P, I64, ctypes.POINTER(c_kv4), I32, I32, P, P], st),
-            "fg_prefill_attn": ([P, I32, I32, I32, I32, ctypes.POINTER(c_kv4), P, P], st),
+            "fg_decode_attn_g4": ([P, I64, ctypes.POINTER(c_kv4), I32, P, I32, P, P], st),
+            "fg_prefill_attn": ([P, I32, I32, I32, I32, P, ctypes.POINTER(c_kv4), P, P], st),
             "fg_layer_workspace_bytes": ([ctypes.POINTER(c_layer), I32, I32, I32, c_policy], SZ),
             "fg_layer_step": ([ctypes.POINTER(c_layer), ctypes.POINTER(c_kv4), P, P, I32, I32,
-                               I32, c_policy, P, SZ, P], st),
+                               I32, P, c_policy, P, SZ, P], st),
             "fg_debug_set": ([I32, I64], st),
             "fg_trace_begin": ([I32], st),
             "fg_trace_end": ([ctypes.POINTER(c_trace_stats)], st),
@@ -132,6 +134,14 @@ def _ptr(t):
         return None
     assert t.is_cuda and t.is_contiguous(), "libfg takes contiguous CUDA tensors"
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _pad(pad, n):
+    """None, or a contiguous int32 CUDA tensor of n left-padding counts."""
+    if pad is None:
+        return None
+    assert pad.dtype == torch.int32 and pad.numel() == n, "pad: int32 tensor of one count per sequence"
+    return _ptr(pad)
 
 
 def _stream(stream=None):
@@ -307,14 +317,24 @@ def fg_layernorm(x, gamma, beta, eps=1e-5, y=None, stream=None, rows=None, x_ld=
     return y
 
 
-def fg_embed(ids, T, pos0, e_tok, e_pos, y=None, stream=None):
+def fg_embed(ids, T, pos0, e_tok, e_pos, y=None, stream=None, pad=None):
     ntok = ids.numel()
     h1 = e_tok.shape[1]
     if y is None:
         y = torch.empty((ntok, h1), dtype=torch.float16, device=e_tok.device)
-    _ok(load().fg_embed(_ptr(ids), ntok, int(T), int(pos0), _ptr(e_tok), e_tok.shape[0],
-                        _ptr(e_pos), e_pos.shape[0], h1, _ptr(y), _stream(stream)))
+    _ok(load().fg_embed(_ptr(ids), ntok, int(T), int(pos0), _pad(pad, ntok // max(int(T), 1)),
+                        _ptr(e_tok), e_tok.shape[0], _ptr(e_pos), e_pos.shape[0], h1, _ptr(y),
+                        _stream(stream)))
     return y
+
+
+def fg_argmax(logits, out=None, stream=None):
+    """Greedy token per row of fp32 logits [B][V] (lowest index among ties)."""
+    B, V = logits.shape
+    if out is None:
+        out = torch.empty(B, dtype=torch.int32, device=logits.device)
+    _ok(load().fg_argmax(_ptr(logits), B, V, _ptr(out), _stream(stream)))
+    return out
 
 
 def fg_kv_append_g4(qkv, cache: KV4, pos, stream=None):
@@ -323,22 +343,23 @@ def fg_kv_append_g4(qkv, cache: KV4, pos, stream=None):
                                _stream(stream)))
 
 
-def fg_decode_attn_g4(qkv, cache: KV4, pos, fuse_append=True, out=None, stream=None):
+def fg_decode_attn_g4(qkv, cache: KV4, pos, fuse_append=True, out=None, stream=None, pad=None):
     if out is None:
         out = torch.empty((qkv.shape[0], cache.H * cache.d), dtype=torch.float16,
                           device=qkv.device)
     c = cache.c()
     _ok(load().fg_decode_attn_g4(_ptr(qkv), qkv.shape[1], ctypes.byref(c), int(pos),
-                                 1 if fuse_append else 0, _ptr(out), _stream(stream)))
+                                 _pad(pad, cache.B), 1 if fuse_append else 0, _ptr(out),
+                                 _stream(stream)))
     return out
 
 
-def fg_prefill_attn(qkv, B, s, H, d, cache: KV4 | None = None, out=None, stream=None):
+def fg_prefill_attn(qkv, B, s, H, d, cache: KV4 | None = None, out=None, stream=None, pad=None):
     if out is None:
         out = torch.empty((B * s, H * d), dtype=torch.float16, device=qkv.device)
     c = None if cache is None else ctypes.byref(cache.c())
-    _ok(load().fg_prefill_attn(_ptr(qkv), int(B), int(s), int(H), int(d), c, _ptr(out),
-                               _stream(stream)))
+    _ok(load().fg_prefill_attn(_ptr(qkv), int(B), int(s), int(H), int(d), _pad(pad, B), c,
+                               _ptr(out), _stream(stream)))
     return out
 
 
@@ -348,8 +369,9 @@ def fg_layer_workspace_bytes(layer_c: c_layer, phase, bls, T, policy: c_policy) 
 
 
 def fg_layer_step(layer_c: c_layer, cache: KV4, x_in, x_out, phase, T, pos,
-                  policy: c_policy, workspace, stream=None):
+                  policy: c_policy, workspace, stream=None, pad=None):
     c = cache.c()
     _ok(load().fg_layer_step(ctypes.byref(layer_c), ctypes.byref(c), _ptr(x_in), _ptr(x_out),
-                             int(phase), int(T), int(pos), policy, _ptr(workspace),
-                             workspace.numel() * workspace.element_size(), _stream(stream)))
+                             int(phase), int(T), int(pos), _pad(pad, cache.B), policy,
+                             _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             _stream(stream)))

@@ -10,6 +10,13 @@ the k batches are one launch per projection (weights read once per block),
 with order "zigzag" they are k launches whose order reverses at every token
 step.  The first generated token comes from the prefill, so n tokens take
 n-1 decode steps.
+
+Prompts of different lengths share a block by left padding to the common
+length s (pad: int32 [bls] counts on the device); positions count from each
+prompt's first real slot and the attention kernels mask the padding, so a
+padded prompt gives the results of the same prompt run alone.  Greedy
+generation feeds back fg_argmax of each step's logits without leaving the
+device.
 """
 from __future__ import annotations
 
@@ -102,8 +109,9 @@ class LayerStack:
             self._ws[key] = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
         return self._ws[key]
 
-    def run(self, x, phase, T, pos, order_code, out=None, stream=None):
-        """x: [bls*T][h1] fp16 -> hidden states after every layer."""
+    def run(self, x, phase, T, pos, order_code, out=None, stream=None, pad=None):
+        """x: [bls*T][h1] fp16 -> hidden states after every layer.  pad: None
+        or int32 [bls] left-padding counts on the device."""
         ws = self.workspace(phase, T, order_code)
         pol = self.policy(order_code)
         bufs = [out if out is not None else torch.empty_like(x), torch.empty_like(x)]
@@ -111,7 +119,8 @@ class LayerStack:
         cur = x
         for j, Lc in enumerate(self.c_layers):
             nxt = bufs[(n - 1 - j) % 2]        # the last layer writes bufs[0]
-            fg.fg_layer_step(Lc, self.caches[j], cur, nxt, phase, T, pos, pol, ws, stream)
+            fg.fg_layer_step(Lc, self.caches[j], cur, nxt, phase, T, pos, pol, ws, stream,
+                             pad=pad)
             cur = nxt
         return cur
 
@@ -132,32 +141,59 @@ class Model:
                             stream=stream)
         return fg.fg_gemm_f16_f32out(h, self.e_tok, Y=logits, stream=stream)
 
-    def prefill(self, prompt_ids, order="block", logits=None, stream=None):
-        """prompt_ids: int32 CUDA [bls][s].  Returns fp32 logits [bls][V] of the
-        last prompt position (the first generated token)."""
+    def prefill(self, prompt_ids, order="block", logits=None, stream=None, pad=None):
+        """prompt_ids: int32 CUDA [bls][s] (left-padded by pad, int32 CUDA [bls]
+        or None).  Returns fp32 logits [bls][V] of the last prompt slot (the
+        first generated token)."""
         bls, s = prompt_ids.shape
-        x = fg.fg_embed(prompt_ids.reshape(-1), s, 0, self.e_tok, self.e_pos, stream=stream)
-        y = self.stack.run(x, fg.FG_PHASE_PREFILL, s, 0, order_for(0, order), stream=stream)
+        x = fg.fg_embed(prompt_ids.reshape(-1), s, 0, self.e_tok, self.e_pos, stream=stream,
+                        pad=pad)
+        y = self.stack.run(x, fg.FG_PHASE_PREFILL, s, 0, order_for(0, order), stream=stream,
+                           pad=pad)
         last = y[s - 1:]          # row b of the view starts at (b*s + s-1) * h1
         return self.head(last, bls, s * self.stack.h1, logits=logits, stream=stream)
 
-    def decode_step(self, ids, t, s, order="block", logits=None, stream=None):
-        """ids: int32 CUDA [bls], fed at position s+t-1 (decode step t >= 1)."""
+    def decode_step(self, ids, t, s, order="block", logits=None, stream=None, pad=None):
+        """ids: int32 CUDA [bls], fed at slot s+t-1 (decode step t >= 1)."""
         pos = s + t - 1
-        x = fg.fg_embed(ids, 1, pos, self.e_tok, self.e_pos, stream=stream)
-        y = self.stack.run(x, fg.FG_PHASE_DECODE, 1, pos, order_for(t, order), stream=stream)
+        x = fg.fg_embed(ids, 1, pos, self.e_tok, self.e_pos, stream=stream, pad=pad)
+        y = self.stack.run(x, fg.FG_PHASE_DECODE, 1, pos, order_for(t, order), stream=stream,
+                           pad=pad)
         return self.head(y, ids.shape[0], self.stack.h1, logits=logits, stream=stream)
 
-    def generate(self, prompt_ids, decode_ids_tm, order="block", stream=None):
+    def generate(self, prompt_ids, decode_ids_tm, order="block", stream=None, pad=None):
         """Teacher-forced generation.  prompt_ids: int32 [bls][s]; decode_ids_tm:
         int32 [D][bls] (time-major, row t-1 fed at decode step t).  Returns
         [logits of the prefill] + [logits of decode step t for t = 1..D], each
         fp32 [bls][V] on the device."""
         s = prompt_ids.shape[1]
-        out = [self.prefill(prompt_ids, order, stream=stream)]
+        out = [self.prefill(prompt_ids, order, stream=stream, pad=pad)]
         for t in range(1, decode_ids_tm.shape[0] + 1):
-            out.append(self.decode_step(decode_ids_tm[t - 1], t, s, order, stream=stream))
+            out.append(self.decode_step(decode_ids_tm[t - 1], t, s, order, stream=stream,
+                                        pad=pad))
         return out
+
+    def generate_greedy(self, prompt_ids, n_new, order="block", stream=None, pad=None,
+                        keep_logits=False):
+        """Greedy generation of n_new tokens per sequence: token 1 is
+        fg_argmax of the prefill's logits, token t+1 fg_argmax of decode step
+        t's logits, fed back at step t; nothing leaves the device.  Returns
+        (tokens int32 [n_new][bls] time-major on the device, the list of
+        logits per step if keep_logits else None)."""
+        bls, s = prompt_ids.shape
+        toks = torch.empty((n_new, bls), dtype=torch.int32, device=prompt_ids.device)
+        keep = [] if keep_logits else None
+        lg = self.prefill(prompt_ids, order, stream=stream, pad=pad)
+        fg.fg_argmax(lg, out=toks[0], stream=stream)
+        if keep is not None:
+            keep.append(lg)
+        for t in range(1, n_new):
+            lg = self.decode_step(toks[t - 1], t, s, order, stream=stream, pad=pad,
+                                  logits=None if keep is not None else lg)
+            fg.fg_argmax(lg, out=toks[t], stream=stream)
+            if keep is not None:
+                keep.append(lg)
+        return toks, keep
 
 
 def random_layers(wl, gen, device="cuda", affine=False, n_layers=None):

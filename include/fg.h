@@ -37,6 +37,17 @@
  *    in the low nibble of byte j and element 2j+1 in the high nibble; meta
  *    is [rows][cols/64][2] fp32 = (min, scale) per group.
  *  - Inputs must be finite; NaN or Inf inputs give unspecified outputs.
+ *  - Left padding (prompts of different lengths in one block, padded to the
+ *    common length s as the pages' workloads are, "FlexGen 完全拆解",
+ *    section on reading the experimental results).  Calls that take
+ *    `const int32_t* pad` accept NULL (no padding) or a DEVICE array of one
+ *    count per sequence, 4-byte aligned: sequence b's prompt occupies slots
+ *    pad[b]..s-1, its tokens take positions counted from slot pad[b],
+ *    every query attends only keys at slots >= pad[b], and prefill queries
+ *    in padding slots output zeros.  A padded prompt gives the results of
+ *    the same prompt run unpadded.  The counts are read on the device and
+ *    cannot be validated on the host: a count outside [0, s) (or, at decode,
+ *    [0, pos]) is clamped into that range, never read out of bounds.
  */
 #ifndef FG_H
 #define FG_H
@@ -208,13 +219,23 @@ fg_status fg_layernorm(const fg_f16* x, int64_t rows, int64_t cols,
                        int64_t x_ld, const fg_f16* gamma, const fg_f16* beta,
                        float eps, fg_f16* y, fg_stream stream);
 
-/* y[r] = e_tok[ids[r]] + e_pos[pos0 + r % T] for r in [0, ntok): the token
- * embedding plus the learned position embedding of sequence-major rows of T
- * tokens starting at position pos0.  ids: [ntok] int32 in [0, vocab).
- * e_tok [vocab][h1], e_pos [npos][h1], y [ntok][h1] fp16; h1 % 8 == 0. */
+/* y[r] = e_tok[ids[r]] + e_pos[p] for r in [0, ntok): the token embedding
+ * plus the learned position embedding of sequence-major rows of T tokens in
+ * slots pos0.., with p = max(pos0 + r % T - pad[r / T], 0) (pad NULL: p =
+ * pos0 + r % T).  ids: [ntok] int32 in [0, vocab).  pad: NULL or [ntok / T].
+ * e_tok [vocab][h1], e_pos [npos][h1], y [ntok][h1] fp16; h1 % 8 == 0;
+ * pos0 + T <= npos. */
 fg_status fg_embed(const int32_t* ids, int64_t ntok, int32_t T, int32_t pos0,
-                   const fg_f16* e_tok, int64_t vocab, const fg_f16* e_pos,
-                   int64_t npos, int32_t h1, fg_f16* y, fg_stream stream);
+                   const int32_t* pad, const fg_f16* e_tok, int64_t vocab,
+                   const fg_f16* e_pos, int64_t npos, int32_t h1, fg_f16* y,
+                   fg_stream stream);
+
+/* Greedy choice of the next token: out[b] = the index of the largest of
+ * logits[b][0..V), the lowest such index when several are equal (so the
+ * result does not depend on the order of the reduction).  logits: [B][V]
+ * fp32, out: [B] int32, both device, 4-byte aligned.  1 <= V < 2^31. */
+fg_status fg_argmax(const float* logits, int64_t B, int64_t V, int32_t* out,
+                    fg_stream stream);
 
 /* ------------------------------------------------------------------ KV cache and attention */
 
@@ -227,32 +248,36 @@ fg_status fg_kv_append_g4(const fg_f16* qkv, int64_t qkv_ld,
                           const fg_kv4* cache, int32_t pos, fg_stream stream);
 
 /* Decode attention over the 4-bit cache: for each sequence b and head h,
- * out = sum_j softmax_j(q . k^_j / sqrt(d)) v^_j over slots j = 0..pos,
- * with k^, v^ the dequantised cache rows.  If fuse_append != 0 the new k, v
- * are first appended into slot pos exactly as fg_kv_append_g4 does (in the
- * same launch).  qkv as for fg_kv_append_g4; out: [B][h1] fp16. */
+ * out = sum_j softmax_j(q . k^_j / sqrt(d)) v^_j over slots j = pad[b]..pos
+ * (pad NULL: 0..pos), with k^, v^ the dequantised cache rows.  If
+ * fuse_append != 0 the new k, v are first appended into slot pos exactly as
+ * fg_kv_append_g4 does (in the same launch).  qkv as for fg_kv_append_g4;
+ * pad: NULL or [B]; out: [B][h1] fp16. */
 fg_status fg_decode_attn_g4(const fg_f16* qkv, int64_t qkv_ld,
                             const fg_kv4* cache, int32_t pos,
-                            int32_t fuse_append, fg_f16* out,
-                            fg_stream stream);
+                            const int32_t* pad, int32_t fuse_append,
+                            fg_f16* out, fg_stream stream);
 
 /* Causal prefill attention for B sequences of s prompt tokens over the fp16
- * K, V straight from the QKV projection: out_i = sum_{j<=i}
- * softmax_j(q_i . k_j / sqrt(d)) v_j.  qkv: [B*s][3*h1] fp16 (sequence-major
- * rows); out: [B*s][h1] fp16.  If cache is not NULL, the K and V rows of
- * every prompt token are also quantised into slots 0..s-1 (s <= cap,
- * cache->B == B, H and d must match). */
+ * K, V straight from the QKV projection: out_i = sum_{pad[b]<=j<=i}
+ * softmax_j(q_i . k_j / sqrt(d)) v_j for slots i >= pad[b], and out_i = 0
+ * for padding slots i < pad[b] (pad NULL: no padding).  qkv: [B*s][3*h1]
+ * fp16 (sequence-major rows); pad: NULL or [B]; out: [B*s][h1] fp16.  If
+ * cache is not NULL, the K and V rows of every slot are also quantised into
+ * slots 0..s-1 (s <= cap, cache->B == B, H and d must match). */
 fg_status fg_prefill_attn(const fg_f16* qkv, int32_t B, int32_t s, int32_t H,
-                          int32_t d, const fg_kv4* cache, fg_f16* out,
-                          fg_stream stream);
+                          int32_t d, const int32_t* pad, const fg_kv4* cache,
+                          fg_f16* out, fg_stream stream);
 
 /* ------------------------------------------------------------------ layer step */
 
 /* One decoder layer for bls = p.gbs * p.k sequences of T new tokens:
  *   h = x + OutProj(Attn(LN1(x)));  y = h + FC2(ReLU(FC1(LN2(h)))).
- * phase FG_PHASE_PREFILL: T = s prompt tokens at positions 0..T-1 (the K/V
- * rows are stored into slots 0..T-1).  phase FG_PHASE_DECODE: T = 1; the new
- * token's K/V are appended at slot pos and attended over slots 0..pos.
+ * phase FG_PHASE_PREFILL: T = s prompt tokens in slots 0..T-1 (the K/V rows
+ * are stored into slots 0..T-1).  phase FG_PHASE_DECODE: T = 1; the new
+ * token's K/V are appended at slot pos and attended over slots pad[b]..pos.
+ * pad: NULL or [bls] left-padding counts (the attention masks; the layer
+ * is otherwise row-wise, so positions enter only through fg_embed).
  * x_in, x_out: [bls*T][h1] fp16, sequence-major rows (may not alias).
  * cache->B must equal bls.  The k GPU batches are rows / cache sequences
  * [i*gbs, (i+1)*gbs).  workspace: device scratch of at least
@@ -261,8 +286,9 @@ size_t fg_layer_workspace_bytes(const fg_layer* w, int32_t phase, int32_t bls,
                                 int32_t T, fg_policy p);
 fg_status fg_layer_step(const fg_layer* w, const fg_kv4* cache,
                         const fg_f16* x_in, fg_f16* x_out, int32_t phase,
-                        int32_t T, int32_t pos, fg_policy p, void* workspace,
-                        size_t ws_bytes, fg_stream stream);
+                        int32_t T, int32_t pos, const int32_t* pad,
+                        fg_policy p, void* workspace, size_t ws_bytes,
+                        fg_stream stream);
 
 /* ------------------------------------------------------------------ tracing */
 

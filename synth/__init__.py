@@ -112,3 +112,11 @@ def embeddings(vocab: int, positions: int, h1: int, gen: torch.Generator,
                device="cpu", std: float = 0.02):
     return (normal_f16((vocab, h1), std, gen, device),
             normal_f16((positions, h1), std, gen, device))
+
+
+def pad_counts(n: int, s: int, gen: torch.Generator, min_len: int = 1, device="cpu") -> torch.Tensor:
+    """Left-padding counts of n prompts padded to the common length s: each
+    real length is uniform in [min_len, s] (a mix of short and full prompts),
+    pad = s - length.  int32 [n]."""
+    lengths = torch.randint(min_len, s + 1, (n,), generator=gen, device=device, dtype=torch.int64)
+    return (s - lengths).to(torch.int32)

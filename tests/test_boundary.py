@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert fg.fg_version() >> 16 == 1
+    assert fg.fg_version() >> 16 == 2
     assert lib.fg_status_str(fg.FG_ERR_TIMEOUT) == b"device wait timed out"
 
 
@@ -59,15 +59,25 @@ def test_host_validation_rejects_without_launch(lib):
     assert lib.fg_dequant_gemm_g4(P(0x3000), 0, ctypes.byref(q), None, None, 0, P(0x4000),
                                   None, 0, None) == fg.FG_OK            # M == 0: no work
     kv = fg.c_kv4(P(0x1000), P(0x2000), P(0x3000), P(0x4000), 2, 2, 96, 8)   # d = 96
-    assert lib.fg_decode_attn_g4(P(0x5000), 576, ctypes.byref(kv), 0, 1, P(0x6000),
+    assert lib.fg_decode_attn_g4(P(0x5000), 576, ctypes.byref(kv), 0, None, 1, P(0x6000),
                                  None) == fg.FG_ERR_UNSUPPORTED
     kv = fg.c_kv4(P(0x1000), P(0x2000), P(0x3000), P(0x4000), 2, 2, 64, 8)
-    assert lib.fg_decode_attn_g4(P(0x5000), 384, ctypes.byref(kv), 8, 1, P(0x6000),
+    assert lib.fg_decode_attn_g4(P(0x5000), 384, ctypes.byref(kv), 8, None, 1, P(0x6000),
                                  None) == fg.FG_ERR_SHAPE               # pos == cap
+    assert lib.fg_decode_attn_g4(P(0x5000), 384, ctypes.byref(kv), 7, P(0x7002), 1, P(0x6000),
+                                 None) == fg.FG_ERR_ALIGN               # pad misaligned
     assert lib.fg_kv_append_g4(P(0x5000), 100, ctypes.byref(kv), 0, None) == fg.FG_ERR_SHAPE
     assert lib.fg_layernorm(P(0x1000), 4, 100, 100, P(0x2000), P(0x3000), 1e-5, P(0x4000),
                             None) == fg.FG_ERR_SHAPE
-    assert lib.fg_prefill_attn(P(0x1000), 1, 4, 2, 80, None, P(0x2000), None) == fg.FG_ERR_UNSUPPORTED
+    assert lib.fg_prefill_attn(P(0x1000), 1, 4, 2, 80, None, None, P(0x2000),
+                               None) == fg.FG_ERR_UNSUPPORTED
+    assert lib.fg_prefill_attn(P(0x1000), 1, 4, 2, 64, P(0x3001), None, P(0x2000),
+                               None) == fg.FG_ERR_ALIGN
+    assert lib.fg_argmax(P(0x1000), 4, 0, P(0x2000), None) == fg.FG_ERR_SHAPE
+    assert lib.fg_argmax(P(0x1000), 4, 10, None, None) == fg.FG_ERR_NULL
+    assert lib.fg_argmax(P(0x1000), 0, 10, None, None) == fg.FG_OK      # B == 0: no work
+    assert lib.fg_embed(P(0x1000), 8, 3, 0, None, P(0x2000), 10, P(0x3000), 16, 64, P(0x4000),
+                        None) == fg.FG_ERR_SHAPE                        # ntok % T != 0
     assert lib.fg_debug_set(99, 1) == fg.FG_ERR_UNSUPPORTED
     assert b"unknown knob" in lib.fg_last_error()
 
@@ -83,16 +93,16 @@ def test_layer_step_validation(lib):
     need = lib.fg_layer_workspace_bytes(ctypes.byref(L), 0, 6, 8, pol)
     assert need > 0
     st = lib.fg_layer_step(ctypes.byref(L), ctypes.byref(kv), P(0x5000), P(0x6000), 0, 8, 0,
-                           pol, P(0x100000), need, None)
+                           None, pol, P(0x100000), need, None)
     assert st == fg.FG_ERR_SHAPE and b"bls" in lib.fg_last_error()
     pol = fg.c_policy(2, 2, 0)
     st = lib.fg_layer_step(ctypes.byref(L), ctypes.byref(kv), P(0x5000), P(0x6000), 1, 2, 0,
-                           pol, P(0x100000), 1 << 30, None)
+                           None, pol, P(0x100000), 1 << 30, None)
     assert st == fg.FG_ERR_SHAPE                              # decode needs T == 1
     st = lib.fg_layer_step(ctypes.byref(L), ctypes.byref(kv), P(0x5000), P(0x6000), 1, 1, 3,
-                           pol, P(0x100000), 16, None)
+                           None, pol, P(0x100000), 16, None)
     assert st == fg.FG_ERR_WORKSPACE
     L.fc1 = q(h2 + 64, h1)
     st = lib.fg_layer_step(ctypes.byref(L), ctypes.byref(kv), P(0x5000), P(0x6000), 1, 1, 3,
-                           pol, P(0x100000), 1 << 30, None)
+                           None, pol, P(0x100000), 1 << 30, None)
     assert st == fg.FG_ERR_SHAPE
