@@ -2,9 +2,10 @@
 generation on GB300, plus the dequant-GEMM TFLOP/s and 4-bit KV-attention
 GB/s measured inside the same timed region.
 
-One step = one whole pass of the hot path over one block: prefill of bls
-prompts (embedding, every layer, final LayerNorm and LM head) followed by the
-n-1 teacher-forced decode steps.  Default workload: OPT-30B-shaped model
+One step = one whole pass of the hot path over one block: greedy generation
+of n tokens per prompt -- prefill of bls prompts (embedding, every layer,
+final LayerNorm, LM head, argmax) followed by n-1 decode steps, each fed the
+previous step's argmax on the device.  Default workload: OPT-30B-shaped model
 (48 layers, h1 7168, 56 heads, h2 28672, vocab 50272), gbs 48 x k 3 =
 bls 144, s 512, n 32, weights and KV cache 4-bit g64, all resident in HBM.
 
@@ -240,18 +241,22 @@ def run_fg(args, ws, rank, local):
     model = random_model(wl, seed=0, device=dev)
     g = synth.generator(1000 + rank, dev)
     prompt = synth.token_ids((wl.bls, wl.s), wl.vocab, g, dev)
-    dec_tm = synth.token_ids((D, wl.bls), wl.vocab, g, dev)
     logits_buf = [torch.empty((wl.bls, wl.vocab), dtype=torch.float32, device=dev)
                   for _ in range(2)]
+    toks = torch.empty((wl.n, wl.bls), dtype=torch.int32, device=dev)   # generated, time-major
 
-    def step(evs=None):
+    def step(evs=None, prompt_ids=prompt):
+        # greedy generation of n tokens per prompt: token 1 from the prefill,
+        # token t+1 from decode step t fed token t; all on the device
         if evs:
             evs[0].record(stream)
-        model.prefill(prompt, args.order, logits=logits_buf[0])
+        lg = model.prefill(prompt_ids, args.order, logits=logits_buf[0])
+        fg.fg_argmax(lg, out=toks[0])
         if evs:
             evs[1].record(stream)
         for t in range(1, D + 1):
-            model.decode_step(dec_tm[t - 1], t, wl.s, args.order, logits=logits_buf[t % 2])
+            lg = model.decode_step(toks[t - 1], t, wl.s, args.order, logits=logits_buf[t % 2])
+            fg.fg_argmax(lg, out=toks[t])
         if evs:
             evs[2].record(stream)
 
@@ -291,33 +296,35 @@ def run_fg(args, ws, rank, local):
     e2e = None
     if not args.no_e2e:
         h_prompt = prompt.cpu().pin_memory()
-        h_dec = dec_tm.cpu().pin_memory()
-        h_logits = torch.empty((wl.bls, wl.vocab), dtype=torch.float32).pin_memory()
+        h_toks = torch.empty((wl.n, wl.bls), dtype=torch.int32).pin_memory()
         d_prompt = torch.empty_like(prompt)
-        d_dec = torch.empty_like(dec_tm)
-        e2e_dec = 0.0
+        e2e_dec = e2e_all = 0.0
         barrier()
         torch.cuda.synchronize()
         for k in range(args.steps):
-            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-            e0.record(stream)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            ev[0].record(stream)
             d_prompt.copy_(h_prompt, non_blocking=True)
-            model.prefill(d_prompt, args.order, logits=logits_buf[0])
-            e1.record(stream)
-            d_dec.copy_(h_dec, non_blocking=True)
-            for t in range(1, D + 1):
-                lg = model.decode_step(d_dec[t - 1], t, wl.s, args.order,
-                                       logits=logits_buf[t % 2])
-                h_logits.copy_(lg, non_blocking=True)
-            e2.record(stream)
+            ev[1].record(stream)
+            step(ev[2:], prompt_ids=d_prompt)
+            h_toks.copy_(toks, non_blocking=True)
+            end = torch.cuda.Event(enable_timing=True)
+            end.record(stream)
             torch.cuda.synchronize()
-            e2e_dec += e1.elapsed_time(e2) / 1e3
+            # the decode phase plus the step's host copies (prompt ids in,
+            # generated tokens out)
+            e2e_dec += (ev[0].elapsed_time(ev[1]) + ev[3].elapsed_time(end)) / 1e3
+            e2e_all += ev[0].elapsed_time(end) / 1e3
         e2e_value, _ = aggregate(wl.bls * D * args.steps, e2e_dec, dev)
+        e2e_gen, _ = aggregate(wl.bls * wl.n * args.steps, e2e_all, dev)
         e2e = {"value": e2e_value, "unit": UNIT,
-               "h2d_bytes_per_step": int(h_prompt.numel() * 4 + h_dec.numel() * 4),
-               "d2h_bytes_per_step": int(D * h_logits.numel() * 4),
-               "note": "decode phase timed from the H2D copy of the step's token ids to the "
-                       "D2H copy of every decode step's logits into pinned host memory"}
+               "h2d_bytes_per_step": int(h_prompt.numel() * 4),
+               "d2h_bytes_per_step": int(h_toks.numel() * 4),
+               "generation_tokens_per_s": e2e_gen,
+               "note": "decode phase plus the step's host copies: the H2D copy of the prompt "
+                       "ids from pinned memory and the D2H copy of the n generated tokens of "
+                       "every sequence into pinned memory; generation_tokens_per_s times the "
+                       "whole step, prefill included"}
         fg.fg_check()
 
     if rank != 0:
@@ -345,7 +352,8 @@ def run_fg(args, ws, rank, local):
                                "weights and KV 4-bit g64 in HBM"
                                % (wl.name, wl.layers, wl.h1, wl.H, wl.h2, wl.vocab, wl.gbs,
                                   wl.k, wl.bls, wl.s, wl.n, D),
-                   "order": args.order, "parallelism": "replicas" if ws > 1 else "single",
+                   "order": args.order, "decoding": "greedy (argmax on the device)",
+                   "parallelism": "replicas" if ws > 1 else "single",
                    "l2": "inputs larger than L2 (weights %.1f GB, KV %.1f GB)"
                          % (sum(L.nbytes_q4 for L in model.stack.layers) / 1e9,
                             sum(c.nbytes for c in model.stack.caches) / 1e9)},
@@ -536,7 +544,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="fg", choices=["fg", "reference"])
     ap.add_argument("--workload", default="opt-30b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--order", default="block", choices=["block", "zigzag"])
-    ap.add_argument("--cpu-seqs", type=int, default=8)
+    ap.add_argument("--cpu-seqs", type=int, default=24)
     ap.add_argument("--ref-seqs", type=int, default=2)
     ap.add_argument("--cpu-frac", type=int, default=1)
     ap.add_argument("--ref-frac", type=int, default=4)
