@@ -403,20 +403,23 @@ def _time_launches(fn, iters, stream):
     return a.elapsed_time(b) / iters / 1e3
 
 
-def gemm_case(M, N, K, iters, dev, seed=0):
-    """One dequant-GEMM launch shape; returns (seconds, TFLOP/s, GB/s)."""
+def gemm_case(M, N, K, iters, dev, seed=0, residual=False):
+    """One dequant-GEMM launch shape with a bias (and, as the decoder's out
+    and fc2 projections have, a residual); returns (seconds, TFLOP/s, GB/s)."""
     from bit_group_quant_gb300 import fg
     g = synth.generator(seed, dev)
     q = fg.fg_quantize_g4(synth.normal_f16((N, K), 0.02, g, dev))
     x = synth.normal_f16((M, K), 1.0, g, dev)
+    b = synth.normal_f16((N,), 0.1, g, dev)
+    r = synth.normal_f16((M, N), 1.0, g, dev) if residual else None
     y = torch.empty((M, N), dtype=torch.float16, device=dev)
     ws_n = fg.fg_dequant_gemm_workspace_bytes(M, N, K)
     ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev)
-    fn = lambda: fg.fg_dequant_gemm_g4(x, q, Y=y, workspace=ws)
+    fn = lambda: fg.fg_dequant_gemm_g4(x, q, bias=b, residual=r, Y=y, workspace=ws)
     sec = _time_launches(fn, iters, torch.cuda.current_stream())
     fg.fg_check()
     flops = 2.0 * M * N * K
-    bytes_ = 0.625 * N * K + 2.0 * M * K + 2.0 * M * N
+    bytes_ = 0.625 * N * K + 2.0 * M * K + 2.0 * M * N * (2.0 if residual else 1.0)
     return sec, flops / sec / 1e12, bytes_ / sec / 1e9
 
 
@@ -463,8 +466,9 @@ def run_micro(args):
     dev = "cuda:0"
     peaks, kind = load_peaks()
     if args.micro == "gemm":
-        sec, tf, gb = gemm_case(args.M, args.N, args.K, args.iters, dev)
+        sec, tf, gb = gemm_case(args.M, args.N, args.K, args.iters, dev, residual=args.residual)
         return {"micro": "dequant_gemm", "M": args.M, "N": args.N, "K": args.K,
+                "residual": args.residual,
                 "ms": sec * 1e3, "tflops": tf, "gbs": gb,
                 "frac_tensor": tf / peaks["bf16_tflops"], "peak_source": kind + " bf16_tflops"}
     if args.micro == "prefill":
@@ -553,6 +557,8 @@ def main(argv=None):
     ap.add_argument("--micro", choices=["gemm", "attn", "prefill", "sweep175b"], default=None,
                     help="time one kernel shape (or the OPT-175B layer sweep) instead")
     ap.add_argument("--M", type=int, default=4096)
+    ap.add_argument("--residual", action="store_true",
+                    help="--micro gemm: add a residual operand (the out and fc2 projections)")
     ap.add_argument("--N", type=int, default=28672)
     ap.add_argument("--K", type=int, default=7168)
     ap.add_argument("--B", type=int, default=144)

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_fp16.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -71,16 +72,37 @@ struct GemmPlan {
     int feat_tiles;  // ceil(N / 128)
     int splits;      // K splits (grid.z); > 1 only when plan_rows fit one token tile
     int kc_per_split;  // K chunks (of 64) per split, a multiple of 4
-    size_t ws_bytes; // fp32 partial sums when splits > 1
+    size_t ws_bytes; // fp32 partial sums (and, for the TMEM kernel, its flags)
+    // the TMEM-operand kernel for one token tile of at most 160 rows
+    // (gemm_dec.cu): clusters of dec_c CTAs share each activation stage;
+    // dec_units = (feature tiles / dec_c) * (K / 256) units dealt out evenly
+    // over dec_Q clusters
+    int dec;
+    int dec_c, dec_Q, dec_nbox;
+    long long dec_units;
+    size_t dec_part_bytes;   // partial sums; the flags follow
 };
-// The summation order of every output -- hence its value -- depends on (N, K)
-// and on whether plan_rows fits one 256-row token tile, never on M itself:
-// launches that must give identical rows (the batches of one block and the
-// whole block) pass the same plan_rows.  plan_rows < M means plan_rows = M.
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int64_t plan_rows = 0);
+// The summation order of every output -- hence its value -- depends on (N, K),
+// the SM count and which kernel plan_rows selects (at most 160 rows with K a
+// multiple of 256: the TMEM kernel; at most 256: one token tile with K split
+// across CTAs; more: whole tiles), never on M itself: launches that must give
+// identical rows (the batches of one block and the whole block) pass the same
+// plan_rows.  plan_rows < M means plan_rows = M.  dequant = false plans the
+// fp16-weight GEMM (no TMEM kernel).
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int64_t plan_rows = 0, bool dequant = true);
 fg_status launch_gemm_g4(const __half* X, int64_t M, const fg_q4* W, const __half* bias,
                          const __half* residual, int act, __half* Y, void* ws, size_t ws_bytes,
                          cudaStream_t st, int64_t plan_rows = 0);
+// gemm_dec.cu: fills the TMEM-kernel fields of pl and returns true when that
+// kernel takes (M, N, K, plan_rows); launches it.
+bool plan_gemm_dec(int64_t M, int64_t N, int64_t K, int64_t plan_rows, GemmPlan& pl);
+fg_status launch_gemm_dec(const __half* X, int64_t M, const fg_q4* W, const __half* bias,
+                          const __half* residual, int act, __half* Y, void* ws, size_t ws_bytes,
+                          cudaStream_t st, const GemmPlan& pl);
+// 2-D row-major tensor map [rows][cols] of `esize`-byte elements, box {bx, by}.
+fg_status make_tmap(CUtensorMap* tm, const void* ptr, CUtensorMapDataType dt, int esize,
+                    uint64_t cols, uint64_t rows, uint32_t bx, uint32_t by,
+                    CUtensorMapSwizzle swz);
 fg_status launch_gemm_f16_f32out(const __half* X, int64_t M, const __half* W, int64_t N,
                                  int64_t K, float* Y, cudaStream_t st);
 
@@ -255,6 +277,17 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T, fp16 inputs, fp32 accumulate: A is 128
+// lanes (rows) x 8 columns (16 fp16 k values, two per 32-bit column) of TMEM.
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Arrive once on an mbarrier when all previously issued tcgen05 ops of this
 // thread have completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -281,8 +314,40 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
+// 32 lanes x 32 bit, 8 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// 32 lanes x 32 bit, 32 consecutive columns per thread.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---- flags between CTAs of one grid (global memory, gpu scope)
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile stored with the
@@ -300,6 +365,32 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 __device__ __forceinline__ uint32_t idesc_f16_f32(int M, int N) {
     return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ---- dequantisation of stored 4-bit codes
+// 8 codes (one 32-bit word, element 0 in the lowest nibble) -> the 8 fp16
+// values fp16(fma(c, s, m)): one fp32 fused multiply-add, then round to
+// nearest even -- the dequantisation of the definition, bit for bit.
+//
+// A code is masked into an fp16 word as the subnormal c * 2^-24 (nibbles 1
+// and 3 of each byte pair are taken in place, as 16c * 2^-24), converted to
+// fp32 exactly, and multiplied by S = s * 2^24 (S16 = s * 2^20): the product
+// is exactly c * s, so the fma rounds c*s + m once, as the definition does.
+// (Scaling s by a power of two is exact: fp16 inputs bound s below 2^14.)
+__device__ __forceinline__ uint4 dequant8(uint32_t w, float S, float S16, float m) {
+    const uint32_t w8 = w >> 8;
+    const uint32_t t0 = w & 0x000F000Fu, t1 = w & 0x00F000F0u;     // (c0, c4), (16c1, 16c5)
+    const uint32_t t2 = w8 & 0x000F000Fu, t3 = w8 & 0x00F000F0u;   // (c2, c6), (16c3, 16c7)
+    const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&t0));
+    const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&t1));
+    const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&t2));
+    const float2 a3 = __half22float2(*reinterpret_cast<const __half2*>(&t3));
+    __half2 h[4];
+    h[0] = __floats2half2_rn(__fmaf_rn(a0.x, S, m), __fmaf_rn(a1.x, S16, m));   // (e0, e1)
+    h[1] = __floats2half2_rn(__fmaf_rn(a2.x, S, m), __fmaf_rn(a3.x, S16, m));   // (e2, e3)
+    h[2] = __floats2half2_rn(__fmaf_rn(a0.y, S, m), __fmaf_rn(a1.y, S16, m));   // (e4, e5)
+    h[3] = __floats2half2_rn(__fmaf_rn(a2.y, S, m), __fmaf_rn(a3.y, S16, m));   // (e6, e7)
+    return *reinterpret_cast<uint4*>(h);
 }
 
 // ---- IEEE total order helpers (finite values): -0 below +0.

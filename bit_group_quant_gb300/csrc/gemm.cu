@@ -88,31 +88,6 @@ struct GemmParams {
     int drop_arrive;
 };
 
-// 8 codes (one 32-bit word, element 0 in the lowest nibble) -> the 8 fp16
-// values fp16(fma(c, s, m)): one fp32 fused multiply-add, then round to
-// nearest even -- the dequantisation of the definition, bit for bit.
-//
-// A code is masked into an fp16 word as the subnormal c * 2^-24 (nibbles 1
-// and 3 of each byte pair are taken in place, as 16c * 2^-24), converted to
-// fp32 exactly, and multiplied by S = s * 2^24 (S16 = s * 2^20): the product
-// is exactly c * s, so the fma rounds c*s + m once, as the definition does.
-// (Scaling s by a power of two is exact: fp16 inputs bound s below 2^14.)
-__device__ __forceinline__ uint4 dequant8(uint32_t w, float S, float S16, float m) {
-    const uint32_t w8 = w >> 8;
-    const uint32_t t0 = w & 0x000F000Fu, t1 = w & 0x00F000F0u;     // (c0, c4), (16c1, 16c5)
-    const uint32_t t2 = w8 & 0x000F000Fu, t3 = w8 & 0x00F000F0u;   // (c2, c6), (16c3, 16c7)
-    const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&t0));
-    const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&t1));
-    const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&t2));
-    const float2 a3 = __half22float2(*reinterpret_cast<const __half2*>(&t3));
-    __half2 h[4];
-    h[0] = __floats2half2_rn(__fmaf_rn(a0.x, S, m), __fmaf_rn(a1.x, S16, m));   // (e0, e1)
-    h[1] = __floats2half2_rn(__fmaf_rn(a2.x, S, m), __fmaf_rn(a3.x, S16, m));   // (e2, e3)
-    h[2] = __floats2half2_rn(__fmaf_rn(a0.y, S, m), __fmaf_rn(a1.y, S16, m));   // (e4, e5)
-    h[3] = __floats2half2_rn(__fmaf_rn(a2.y, S, m), __fmaf_rn(a3.y, S16, m));   // (e6, e7)
-    return *reinterpret_cast<uint4*>(h);
-}
-
 // Dequantiser index 0..7 of a warp (-1 for other warps).  Sub-partition 1
 // (warps 1, 5, 9) is left to the single MMA-issuing thread during the
 // mainloop: every instruction on its path is latency-critical.
@@ -481,6 +456,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, r);
             tmem_wait_ld();
             if (!live || n >= p.N) continue;
+            // residual loads are all issued before the first store (the
+            // residual never aliases Y), so their latencies overlap
+            float res[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int m = tok0 + c0 + j;
+                res[j] = (!kF32Out && gridDim.z == 1 && p.residual != nullptr && m < p.M)
+                             ? __half2float(__ldg(p.residual + static_cast<int64_t>(m) * p.N + n))
+                             : 0.0f;
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int m = tok0 + c0 + j;
@@ -494,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     float v = __fadd_rn(acc, bias);
                     if (p.act == FG_ACT_RELU) v = fmaxf(v, 0.0f);
-                    if (p.residual) v = __fadd_rn(v, __half2float(p.residual[idx]));
+                    if (p.residual) v = __fadd_rn(v, res[j]);
                     p.Y[idx] = __float2half_rn(v);
                 }
             }
@@ -552,38 +537,6 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// 2-D row-major tensor [rows][cols] of `esize`-byte elements; box = {bx, by}.
-fg_status make_tmap(CUtensorMap* tm, const void* ptr, CUtensorMapDataType dt, int esize,
-                    uint64_t cols, uint64_t rows, uint32_t bx, uint32_t by,
-                    CUtensorMapSwizzle swz) {
-    auto fn = encode_fn();
-    if (!fn) return fg::set_error(FG_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * static_cast<uint64_t>(esize)};
-    cuuint32_t box[2] = {bx, by};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(tm, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS)
-        return fg::set_error(FG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
-    return FG_OK;
-}
-
 struct Rings {
     int ns, sc;
     size_t smem;
@@ -628,7 +581,7 @@ fg_status run_gemm(const void* X, const CUtensorMap& tmW, GemmParams& p, const f
     p.feat_tiles = plan.feat_tiles;
     p.tok_tiles = plan.tok_tiles;
     CUtensorMap tmX;
-    fg_status s = make_tmap(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.K, p.M, kChunk,
+    fg_status s = fg::make_tmap(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.K, p.M, kChunk,
                             plan.nt / p.cluster, CU_TENSOR_MAP_SWIZZLE_128B);
     if (s != FG_OK) return s;
     auto kern = gemm_tc_kernel<kDequant, kF32Out>;
@@ -666,13 +619,49 @@ fg_status run_gemm(const void* X, const CUtensorMap& tmW, GemmParams& p, const f
 
 namespace fg {
 
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+fg_status make_tmap(CUtensorMap* tm, const void* ptr, CUtensorMapDataType dt, int esize,
+                    uint64_t cols, uint64_t rows, uint32_t bx, uint32_t by,
+                    CUtensorMapSwizzle swz) {
+    auto fn = encode_fn();
+    if (!fn) return fg::set_error(FG_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * static_cast<uint64_t>(esize)};
+    cuuint32_t box[2] = {bx, by};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(tm, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fg::set_error(FG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return FG_OK;
+}
+
+
 // Tile plan.  It depends on M only through the number of 256-row activation
 // tiles, and the K split only on (N, K) -- and is used only when all rows fit
 // one tile -- so every row's result is independent of M and of the other rows
 // (the row-by-row and zig-zag block orders must agree bit for bit).
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int64_t plan_rows) {
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int64_t plan_rows, bool dequant) {
     GemmPlan pl{};
     if (plan_rows < M) plan_rows = M;
+    if (dequant && plan_gemm_dec(M, N, K, plan_rows, pl)) return pl;
     pl.tok_tiles = static_cast<int>(cdiv(M, 256));
     if (pl.tok_tiles < 1) pl.tok_tiles = 1;
     int64_t rows = cdiv(M, pl.tok_tiles);
@@ -709,6 +698,7 @@ fg_status launch_gemm_g4(const __half* X, int64_t M, const fg_q4* W, const __hal
     if (pl.ws_bytes > 0 && (ws == nullptr || ws_bytes < pl.ws_bytes))
         return set_error(FG_ERR_WORKSPACE, "dequant_gemm: workspace %zu < %zu bytes", ws_bytes,
                          pl.ws_bytes);
+    if (pl.dec) return launch_gemm_dec(X, M, W, bias, residual, act, Y, ws, ws_bytes, st, pl);
     // codes: one box = 128 rows x 128 bytes (4 K chunks), 128-byte swizzle
     CUtensorMap tmC;
     fg_status s = make_tmap(&tmC, W->codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N,
@@ -744,7 +734,7 @@ fg_status launch_gemm_g4(const __half* X, int64_t M, const fg_q4* W, const __hal
 fg_status launch_gemm_f16_f32out(const __half* X, int64_t M, const __half* W, int64_t N,
                                  int64_t K, float* Y, cudaStream_t st) {
     if (M == 0) return FG_OK;
-    GemmPlan pl = plan_gemm(M, N, K);
+    GemmPlan pl = plan_gemm(M, N, K, M, false);
     pl.splits = 1;
     CUtensorMap tmW;
     fg_status s = make_tmap(&tmW, W, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, K, N, kChunk, kTileF,
