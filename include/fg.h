@@ -171,9 +171,12 @@ fg_status fg_dequant_g4(const fg_q4* in, fg_f16* x, fg_stream stream);
  * Each output is fp32-accumulated fp16(x) * fp16(w^) products with
  * w^ = fp16(fma(q, scale, min)) exactly as fg_dequant_g4 gives it.  The
  * result of a row never depends on the other rows; it depends on M only
- * through one switch -- whether M <= 256 (then K may be split across CTAs
- * and summed in a fixed order) -- so launches of 1..256 rows agree bit for
- * bit, as do launches of more than 256 rows. */
+ * through which of three regimes M falls in -- at most 144 rows with K a
+ * multiple of 256 (the dequantised weights go to TMEM and K is split over
+ * persistent CTA clusters, parts summed in a fixed order), at most 256 rows
+ * (K split across CTAs, fixed-order sum), more than 256 rows (whole tiles) --
+ * so launches in the same regime agree bit for bit.  The K split depends on
+ * (N, K) and the device's SM count. */
 size_t fg_dequant_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 fg_status fg_dequant_gemm_g4(const fg_f16* X, int64_t M, const fg_q4* W,
                              const fg_f16* bias, const fg_f16* residual,
