@@ -238,7 +238,8 @@ def run_fg(args, ws, rank, local):
     init_dist(ws, "nccl")
     stream = torch.cuda.current_stream()
 
-    model = random_model(wl, seed=0, device=dev)
+    host = args.weights == "host"
+    model = random_model(wl, seed=0, device=dev, host_weights=host)
     g = synth.generator(1000 + rank, dev)
     prompt = synth.token_ids((wl.bls, wl.s), wl.vocab, g, dev)
     logits_buf = [torch.empty((wl.bls, wl.vocab), dtype=torch.float32, device=dev)
@@ -327,10 +328,38 @@ def run_fg(args, ws, rank, local):
                        "whole step, prefill included"}
         fg.fg_check()
 
+    stream_info = None
+    if host:
+        # beta: one layer's weight copies alone (the copy stream idle otherwise)
+        torch.cuda.synchronize()
+        st = model.stack
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        a.record(st.copy_stream)
+        for r in range(reps):
+            st.next = None
+            st._fetch(r % len(st.layers), r % 2)
+        b.record(st.copy_stream)
+        torch.cuda.synchronize()
+        st.next = None
+        beta = st.bytes_per_layer * reps / (a.elapsed_time(b) / 1e3)
+        W = st.bytes_per_layer * len(st.layers)
+        t_step = t_dec / max(args.steps, 1) / D
+        stream_info = {
+            "bytes_per_layer": st.bytes_per_layer, "model_bytes": W,
+            "h2d_gbs": beta / 1e9,
+            "bound_ms_per_decode_step": W / beta * 1e3,
+            "measured_ms_per_decode_step": t_step * 1e3,
+            "note": "weights fetched once per token step for the whole block: per sequence at "
+                    "least W/(B beta); the decode step is bound by W/beta when that exceeds "
+                    "the resident step's compute"}
+
     if rank != 0:
         return None
 
     peaks, peak_kind = load_peaks()
+    wbytes = (model.stack.bytes_per_layer * len(model.stack.layers) if host
+              else sum(L.nbytes_q4 for L in model.stack.layers))
     gp = trace["gemm_prefill"]
     gd = trace["gemm_decode"]
     ad = trace["attn_decode"]
@@ -354,9 +383,10 @@ def run_fg(args, ws, rank, local):
                                   wl.k, wl.bls, wl.s, wl.n, D),
                    "order": args.order, "decoding": "greedy (argmax on the device)",
                    "parallelism": "replicas" if ws > 1 else "single",
+                   "weights": ("4-bit, pinned host memory, streamed one layer ahead over "
+                               "NVLink-C2C" if host else "4-bit, resident in HBM"),
                    "l2": "inputs larger than L2 (weights %.1f GB, KV %.1f GB)"
-                         % (sum(L.nbytes_q4 for L in model.stack.layers) / 1e9,
-                            sum(c.nbytes for c in model.stack.caches) / 1e9)},
+                         % (wbytes / 1e9, sum(c.nbytes for c in model.stack.caches) / 1e9)},
         "generation_tokens_per_s": gen_value,
         "gemm_tflops": {"prefill": tflops(gp), "decode": tflops(gd)},
         "attn_gbs": {"decode_4bit": gbs(ad)},
@@ -378,6 +408,7 @@ def run_fg(args, ws, rank, local):
                      "frac": gbs(ad) / peaks["hbm_gbs"] if gbs(ad) else None}},
         "prefill_attn_tflops": tflops(ap),
         "cpu_baseline": cpu_base,
+        "weight_stream": stream_info,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk,
@@ -461,10 +492,49 @@ def prefill_case(B, s, H, d, iters, dev, seed=0):
     return sec, flops / sec / 1e12
 
 
+def decode_case(args, dev):
+    """Decode steps only (greedy, block order) of the workload's model at
+    bls = gbs * k, weights resident in HBM or streamed from pinned host
+    memory: decode tokens/s.  The prompt's cache rows are left as allocated
+    (zeros): a decode step's work does not depend on the cache contents."""
+    import dataclasses
+    from bit_group_quant_gb300 import fg
+    from bit_group_quant_gb300.model import random_model
+    wl = synth.WORKLOADS[args.workload]
+    if args.gbs:
+        wl = dataclasses.replace(wl, gbs=args.gbs, k=args.k or 1)
+    host = args.weights == "host"
+    model = random_model(wl, seed=0, device=dev, host_weights=host)
+    D = wl.decode_steps
+    toks = torch.zeros((wl.n, wl.bls), dtype=torch.int32, device=dev)
+    lg = [torch.empty((wl.bls, wl.vocab), dtype=torch.float32, device=dev) for _ in range(2)]
+    def steps(n):
+        for t in range(1, n + 1):
+            l = model.decode_step(toks[t - 1], t, wl.s, "block", logits=lg[t % 2])
+            fg.fg_argmax(l, out=toks[t])
+    steps(3)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    h0 = time.perf_counter()
+    steps(D)
+    h1 = time.perf_counter()
+    b.record()
+    torch.cuda.synchronize()
+    fg.fg_check()
+    sec = a.elapsed_time(b) / 1e3
+    return {"micro": "decode", "weights": args.weights, "bls": wl.bls, "gbs": wl.gbs, "k": wl.k,
+            "decode_steps": D, "ms_per_decode_step": sec / D * 1e3,
+            "host_enqueue_ms_per_decode_step": (h1 - h0) / D * 1e3,
+            "decode_tokens_per_s": wl.bls * D / sec}
+
+
 def run_micro(args):
     torch.cuda.set_device(0)
     dev = "cuda:0"
     peaks, kind = load_peaks()
+    if args.micro == "decode":
+        return decode_case(args, dev)
     if args.micro == "gemm":
         sec, tf, gb = gemm_case(args.M, args.N, args.K, args.iters, dev, residual=args.residual)
         return {"micro": "dequant_gemm", "M": args.M, "N": args.N, "K": args.K,
@@ -548,13 +618,17 @@ def main(argv=None):
     ap.add_argument("--impl", default="fg", choices=["fg", "reference"])
     ap.add_argument("--workload", default="opt-30b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--order", default="block", choices=["block", "zigzag"])
+    ap.add_argument("--weights", default="hbm", choices=["hbm", "host"],
+                    help="host: 4-bit weights in pinned host memory, streamed one layer ahead")
     ap.add_argument("--cpu-seqs", type=int, default=24)
     ap.add_argument("--ref-seqs", type=int, default=2)
     ap.add_argument("--cpu-frac", type=int, default=1)
     ap.add_argument("--ref-frac", type=int, default=4)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--micro", choices=["gemm", "attn", "prefill", "sweep175b"], default=None,
+    ap.add_argument("--gbs", type=int, default=0, help="--micro decode: override gbs")
+    ap.add_argument("--k", type=int, default=0, help="--micro decode: override k")
+    ap.add_argument("--micro", choices=["gemm", "attn", "prefill", "sweep175b", "decode"], default=None,
                     help="time one kernel shape (or the OPT-175B layer sweep) instead")
     ap.add_argument("--M", type=int, default=4096)
     ap.add_argument("--residual", action="store_true",

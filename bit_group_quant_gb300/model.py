@@ -209,11 +209,140 @@ def random_layers(wl, gen, device="cuda", affine=False, n_layers=None):
     return layers
 
 
-def random_model(wl, seed=0, device="cuda", n_layers=None, cap=None):
+def random_model(wl, seed=0, device="cuda", n_layers=None, cap=None, host_weights=False):
+    """host_weights: keep the 4-bit weights in pinned host memory and stream
+    them one layer ahead (HostLayerStack)."""
     gen = synth.generator(seed, device)
     layers = random_layers(wl, gen, device, n_layers=n_layers)
-    stack = LayerStack(layers, wl.gbs, wl.k, cap or wl.cap, device)
+    cls = HostLayerStack if host_weights else LayerStack
+    stack = cls(layers, wl.gbs, wl.k, cap or wl.cap, device)
     e_tok, e_pos = synth.embeddings(wl.vocab, wl.cap, wl.h1, gen, device)
     ones = torch.ones(wl.h1, dtype=torch.float16, device=device)
     zeros = torch.zeros(wl.h1, dtype=torch.float16, device=device)
     return Model(stack, e_tok, e_pos, ones, zeros)
+
+
+class HostLayerStack(LayerStack):
+    """A LayerStack whose 4-bit weights live in pinned host memory and are
+    streamed to the GPU one layer ahead ("FlexGen 完全拆解", section on how
+    the three data paths overlap: while the k batches of a block run on layer
+    j, the weights of layer j+1 are fetched; the weight-read bound per
+    sequence is W / (B beta), section on the problem).
+
+    Each layer's four projections (codes and min/scale pairs) are packed into
+    one pinned host buffer, at 1 KB-aligned offsets, so that a fetch is a
+    single asynchronous copy.  Two device buffers of that size form a ring.
+    A copy stream fetches the next layer into the buffer the previous layer
+    released: each copy waits for the compute that last read its buffer, and
+    each layer's compute waits for its copy.  The last layer's successor is
+    layer 0 of the next token step, so the fetch runs across step boundaries
+    too.  Biases, LayerNorm parameters and the KV cache stay on the device.
+    Results are bit-identical to the resident stack (same kernels, same
+    bytes)."""
+
+    NAMES = ("qkv", "out", "fc1", "fc2")
+    ALIGN = 1024
+
+    @classmethod
+    def _layout(cls, L0):
+        """(name, codes offset, meta offset, rows, cols) per projection, and
+        the packed size in bytes."""
+        lay, off = [], 0
+        up = lambda v: (v + cls.ALIGN - 1) // cls.ALIGN * cls.ALIGN
+        for nm in cls.NAMES:
+            q = getattr(L0, nm)
+            oc = off
+            om = up(oc + q.codes.numel())
+            off = up(om + q.meta.numel() * 4)
+            lay.append((nm, oc, om, q.rows, q.cols))
+        return lay, off
+
+    @staticmethod
+    def _views(buf, lay):
+        out = {}
+        for nm, oc, om, rows, cols in lay:
+            codes = buf[oc:oc + rows * cols // 2].view(rows, cols // 2)
+            meta = buf[om:om + rows * cols // 64 * 8].view(torch.float32).view(rows, cols // 64, 2)
+            out[nm] = fg.Q4(codes, meta, rows, cols)
+        return out
+
+    def __init__(self, layers, gbs: int, k: int, cap: int, device="cuda"):
+        L0 = layers[0]
+        self.layout, self.bytes_per_layer = self._layout(L0)
+        # host copies of the quantised projections, one pinned buffer per
+        # layer; the device copies are dropped
+        self.host = []
+        for L in layers:
+            hb = torch.empty(self.bytes_per_layer, dtype=torch.uint8).pin_memory()
+            hv = self._views(hb, self.layout)
+            for nm in self.NAMES:
+                hv[nm].codes.copy_(getattr(L, nm).codes)
+                hv[nm].meta.copy_(getattr(L, nm).meta)
+                setattr(L, nm, None)
+            self.host.append(hb)
+        self.layers = list(layers)
+        self.dev = [torch.empty(self.bytes_per_layer, dtype=torch.uint8, device=device)
+                    for _ in range(2)]
+        self.buf = [self._views(b, self.layout) for b in self.dev]
+        self.gbs, self.k, self.cap = gbs, k, cap
+        self.h1, self.H, self.h2 = L0.h1, L0.H, L0.h2
+        self.d = self.h1 // self.H
+        self.device = device
+        self.caches = [fg.KV4.empty(self.bls, self.H, self.d, cap, device) for _ in layers]
+        self._ws = {}
+        self.copy_stream = torch.cuda.Stream(device)
+        self.freed = [torch.cuda.Event(), torch.cuda.Event()]
+        self.fetched = [torch.cuda.Event(), torch.cuda.Event()]
+        self.next = None          # (layer, slot): the fetch already issued
+        # the C layer descriptors, one per (layer, slot)
+        self.c_slot = [[self._c_layer(j, s) for s in range(2)] for j in range(len(layers))]
+        self.c_layers = None
+
+    def _c_layer(self, j, slot):
+        L = self.layers[j]
+        b = self.buf[slot]
+        p = lambda t: t.data_ptr()
+        return fg.c_layer(b["qkv"].c(), b["out"].c(), b["fc1"].c(), b["fc2"].c(),
+                          p(L.b_qkv), p(L.b_out), p(L.b_fc1), p(L.b_fc2),
+                          p(L.ln1_g), p(L.ln1_b), p(L.ln2_g), p(L.ln2_b),
+                          L.h1, L.H, L.h2, L.eps)
+
+    def _fetch(self, j, slot):
+        """Issue the copy of layer j's weights into device slot `slot`."""
+        cp = self.copy_stream
+        cp.wait_event(self.freed[slot])   # its last reader has finished
+        with torch.cuda.stream(cp):
+            self.dev[slot].copy_(self.host[j], non_blocking=True)
+        self.fetched[slot].record(cp)
+
+    def workspace(self, phase, T, order_code):
+        key = (phase, T, order_code != fg.FG_ORDER_BLOCK)
+        if key not in self._ws:
+            n = fg.fg_layer_workspace_bytes(self.c_slot[0][0], phase, self.bls, T,
+                                            self.policy(order_code))
+            self._ws[key] = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+        return self._ws[key]
+
+    def run(self, x, phase, T, pos, order_code, out=None, stream=None, pad=None):
+        cs = stream if stream is not None else torch.cuda.current_stream()
+        ws = self.workspace(phase, T, order_code)
+        pol = self.policy(order_code)
+        n = len(self.layers)
+        bufs = [out if out is not None else torch.empty_like(x), torch.empty_like(x)]
+        if self.next is None:
+            self._fetch(0, 0)
+            self.next = (0, 0)
+        cur = x
+        for j in range(n):
+            lj, slot = self.next
+            assert lj == j
+            cs.wait_event(self.fetched[slot])
+            nj = (j + 1) % n
+            self._fetch(nj, 1 - slot)
+            self.next = (nj, 1 - slot)
+            nxt = bufs[(n - 1 - j) % 2]
+            fg.fg_layer_step(self.c_slot[j][slot], self.caches[j], cur, nxt, phase, T, pos, pol,
+                             ws, cs, pad=pad)
+            self.freed[slot].record(cs)
+            cur = nxt
+        return cur
