@@ -86,6 +86,9 @@ def _load():
                 "or_kv_store_prefill": ([P, I32, I32, P, P, P, P, I32, I32, I32], None),
                 "or_prefill_attn": ([P, I32, I32, I32, I32, P, P], None),
                 "or_decode_attn_g4": ([P, I64, P, P, P, P, I32, I32, I32, I32, I32, I32, P, P], None),
+                "or_decode_attn_topk_g4": ([P, I64, P, P, P, P, I32, I32, I32, I32, I32, I32, P,
+                                            I32, P, P, P], None),
+                "or_topk_count": ([I64, I32], I32),
                 "or_argmax": ([P, I64, I64, P], None),
             }
             for name, (args, res) in sig.items():
@@ -301,6 +304,35 @@ def decode_attn_g4(qkv, cache: KVCache, pos, append=True, pad=None):
                               cache.H, cache.d, cache.cap, int(pos),
                               1 if append else 0, None if pad is None else _p(pad), _p(out))
     return out
+
+
+def topk_count(n, keep_pct):
+    """Rows kept out of n by top-K sparse attention at keep_pct percent."""
+    return int(_load().or_topk_count(int(n), int(keep_pct)))
+
+
+def decode_attn_topk_g4(qkv, cache: KVCache, pos, keep_pct, append=True, pad=None, sel=None):
+    """Top-K sparse decode attention (full softmax, only the keep_pct percent
+    highest-scoring rows' V summed).  sel: None, or [B][H][kmax] int32 kept
+    slots to use instead of the oracle's own choice.  Returns (out, sel_used)
+    with sel_used [B][H][kmax] (-1 past a sequence's own count)."""
+    qkv = _c(qkv, np.float16)
+    B = qkv.shape[0]
+    assert B == cache.B and 0 <= pos < cache.cap and 1 <= keep_pct <= 100
+    H = cache.H
+    kmax = topk_count(pos + 1, keep_pct)
+    out = np.empty((B, H * cache.d), np.float16)
+    sel_out = np.empty((B, H, kmax), np.int32)
+    if sel is not None:
+        sel = _c(sel, np.int32)
+        assert sel.shape == (B, H, kmax)
+    kc, vc, km, vm = cache._ptrs()
+    pad = _pad(pad, B)
+    _load().or_decode_attn_topk_g4(_p(qkv), qkv.shape[1], kc, vc, km, vm, cache.B, H, cache.d,
+                                   cache.cap, int(pos), 1 if append else 0,
+                                   None if pad is None else _p(pad), int(keep_pct),
+                                   None if sel is None else _p(sel), _p(sel_out), _p(out))
+    return out, sel_out
 
 
 def argmax(logits):

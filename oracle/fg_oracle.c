@@ -493,6 +493,116 @@ void or_decode_attn_g4(const uint16_t* qkv, int64_t qkv_ld, uint8_t* k_codes,
     }
 }
 
+/* Number of rows kept by top-K sparse attention over n attended rows: the
+ * keep_pct percent with the highest scores, rounded up (at least one row). */
+int32_t or_topk_count(int64_t n, int32_t keep_pct)
+{
+    return (int32_t)((n * keep_pct + 99) / 100);
+}
+
+/* Order for the top-K choice: higher score first; equal scores (+0 and -0
+ * compare equal) by ascending slot. */
+static const float* g_rank_sc;
+static int rank_cmp(const void* a, const void* b)
+{
+    int64_t i = *(const int64_t*)a, j = *(const int64_t*)b;
+    float si = g_rank_sc[i], sj = g_rank_sc[j];
+    if (si > sj) return -1;
+    if (si < sj) return 1;
+    return i < j ? -1 : (i > j ? 1 : 0);
+}
+static int slot_cmp(const void* a, const void* b)
+{
+    int64_t i = *(const int64_t*)a, j = *(const int64_t*)b;
+    return i < j ? -1 : (i > j ? 1 : 0);
+}
+
+/* Top-K sparse decode attention over the 4-bit cache ("FlexGen 完全拆解",
+ * section on the paper's further approximations: the attention scores are
+ * computed from every cached key, and only the V rows of the highest-scoring
+ * keep_pct percent are loaded).  Readings: the softmax is the full one over
+ * all n attended rows (maximum and normaliser over every score); the rows not
+ * kept contribute nothing to the weighted sum (no renormalisation); the count
+ * kept is or_topk_count(n, keep_pct); equal scores are kept lowest slot
+ * first; the new token's row is a candidate like any other.  Scores are
+ * computed exactly as or_decode_attn_g4 computes them.
+ * sel_in: NULL, or the kept slots to use instead of the oracle's own choice,
+ * [B][H][kmax] (kmax = or_topk_count(pos+1, keep_pct)), each (b,h) list
+ * ascending and -1 after its own count -- so the weighted sum can be checked
+ * on another implementation's choice.  sel_out: NULL or [B][H][kmax], the
+ * kept slots in that layout.  keep_pct in 1..100; 100 keeps every row and
+ * equals or_decode_attn_g4. */
+void or_decode_attn_topk_g4(const uint16_t* qkv, int64_t qkv_ld, uint8_t* k_codes,
+                            uint8_t* v_codes, float* k_meta, float* v_meta,
+                            int32_t B, int32_t H, int32_t d, int32_t cap,
+                            int32_t pos, int32_t do_append, const int32_t* pad,
+                            int32_t keep_pct, const int32_t* sel_in,
+                            int32_t* sel_out, uint16_t* out)
+{
+    or_kv4 c = {k_codes, v_codes, k_meta, v_meta, B, H, d, cap};
+    int64_t h1 = (int64_t)H * d, L = (int64_t)pos + 1;
+    int64_t kmax = or_topk_count(L, keep_pct);
+    float scale = 1.0f / sqrtf((float)d);
+    if (do_append)
+        for (int64_t b = 0; b < B; ++b)
+            store_kv_row(&c, qkv + b * qkv_ld, b, pos);
+    float* q = (float*)malloc(sizeof(float) * (size_t)d);
+    float* kr = (float*)malloc(sizeof(float) * (size_t)d);
+    float* vr = (float*)malloc(sizeof(float) * (size_t)d);
+    float* sc = (float*)malloc(sizeof(float) * (size_t)L);
+    float* p = (float*)malloc(sizeof(float) * (size_t)L);
+    float* acc = (float*)malloc(sizeof(float) * (size_t)d);
+    int64_t* idx = (int64_t*)malloc(sizeof(int64_t) * (size_t)L);
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t h = 0; h < H; ++h) {
+            const int64_t p0 = pad ? pad[b] : 0, n = L - p0;
+            const int64_t ksel = or_topk_count(n, keep_pct);
+            or_h2f_array(qkv + b * qkv_ld + h * d, q, d);
+            for (int64_t j = 0; j < n; ++j) {
+                load_cache_row(&c, 0, b, h, p0 + j, kr);
+                float dot = 0.0f;
+                for (int64_t i = 0; i < d; ++i) dot += q[i] * kr[i];
+                sc[j] = dot * scale;
+            }
+            /* the full softmax over all n rows */
+            float mx = sc[0];
+            for (int64_t j = 1; j < n; ++j)
+                if (sc[j] > mx) mx = sc[j];
+            float l = 0.0f;
+            for (int64_t j = 0; j < n; ++j) {
+                p[j] = expf(sc[j] - mx);
+                l += p[j];
+            }
+            /* the kept rows, as offsets from slot p0, ascending */
+            const int32_t* given = sel_in ? sel_in + (b * H + h) * kmax : NULL;
+            if (given) {
+                for (int64_t r = 0; r < ksel; ++r) idx[r] = given[r] - p0;
+            } else {
+                for (int64_t j = 0; j < n; ++j) idx[j] = j;
+                g_rank_sc = sc;
+                qsort(idx, (size_t)n, sizeof(int64_t), rank_cmp);
+                qsort(idx, (size_t)ksel, sizeof(int64_t), slot_cmp);
+            }
+            for (int64_t i = 0; i < d; ++i) acc[i] = 0.0f;
+            for (int64_t r = 0; r < ksel; ++r) {
+                load_cache_row(&c, 1, b, h, p0 + idx[r], vr);
+                for (int64_t i = 0; i < d; ++i) acc[i] += p[idx[r]] * vr[i];
+            }
+            for (int64_t i = 0; i < d; ++i) out[b * h1 + h * d + i] = or_f2h(acc[i] / l);
+            if (sel_out) {
+                int32_t* so = sel_out + (b * H + h) * kmax;
+                for (int64_t r = 0; r < kmax; ++r) so[r] = r < ksel ? (int32_t)(p0 + idx[r]) : -1;
+            }
+        }
+    free(q);
+    free(kr);
+    free(vr);
+    free(sc);
+    free(p);
+    free(acc);
+    free(idx);
+}
+
 /* Greedy choice: for each of B rows of V fp32 logits, the index of the
  * largest value (the lowest such index when several are equal). */
 void or_argmax(const float* logits, int64_t B, int64_t V, int32_t* out)
