@@ -454,9 +454,11 @@ def gemm_case(M, N, K, iters, dev, seed=0, residual=False):
     return sec, flops / sec / 1e12, bytes_ / sec / 1e9
 
 
-def attn_case(B, H, d, L, iters, dev, seed=0):
+def attn_case(B, H, d, L, iters, dev, seed=0, topk=0):
     """One decode-attention launch over a full 4-bit cache of L rows
-    (fused append at slot L-1); returns (seconds, GB/s)."""
+    (fused append at slot L-1); returns (seconds, GB/s).  topk 1..99: the
+    top-K sparse attention keeping that percent of the rows' V (its bytes:
+    every K row, the kept V rows)."""
     from bit_group_quant_gb300 import fg
     g = synth.generator(seed, dev)
     cache = fg.KV4.empty(B, H, d, L, dev, zero=False)
@@ -470,11 +472,16 @@ def attn_case(B, H, d, L, iters, dev, seed=0):
     del rows, kq, vq
     qkv = synth.normal_f16((B, 3 * H * d), 1.0, g, dev)
     out = torch.empty((B, H * d), dtype=torch.float16, device=dev)
-    fn = lambda: fg.fg_decode_attn_g4(qkv, cache, L - 1, fuse_append=True, out=out)
+    if 0 < topk < 100:
+        fn = lambda: fg.fg_decode_attn_topk_g4(qkv, cache, L - 1, topk, fuse_append=True, out=out)
+        nv = fg.fg_topk_count(L, topk)
+    else:
+        fn = lambda: fg.fg_decode_attn_g4(qkv, cache, L - 1, fuse_append=True, out=out)
+        nv = L
     sec = _time_launches(fn, iters, torch.cuda.current_stream())
     fg.fg_check()
     row = d / 2 + (d / 64) * 8
-    bytes_ = B * H * (2.0 * L * row + 2 * row + 8.0 * d)
+    bytes_ = B * H * ((L + nv) * row + 2 * row + 8.0 * d)
     return sec, bytes_ / sec / 1e9
 
 
@@ -505,6 +512,7 @@ def decode_case(args, dev):
         wl = dataclasses.replace(wl, gbs=args.gbs, k=args.k or 1)
     host = args.weights == "host"
     model = random_model(wl, seed=0, device=dev, host_weights=host)
+    model.stack.topk_pct = args.topk
     D = wl.decode_steps
     toks = torch.zeros((wl.n, wl.bls), dtype=torch.int32, device=dev)
     lg = [torch.empty((wl.bls, wl.vocab), dtype=torch.float32, device=dev) for _ in range(2)]
@@ -523,7 +531,8 @@ def decode_case(args, dev):
     torch.cuda.synchronize()
     fg.fg_check()
     sec = a.elapsed_time(b) / 1e3
-    return {"micro": "decode", "weights": args.weights, "bls": wl.bls, "gbs": wl.gbs, "k": wl.k,
+    return {"micro": "decode", "weights": args.weights, "topk_pct": args.topk,
+            "bls": wl.bls, "gbs": wl.gbs, "k": wl.k,
             "decode_steps": D, "ms_per_decode_step": sec / D * 1e3,
             "host_enqueue_ms_per_decode_step": (h1 - h0) / D * 1e3,
             "decode_tokens_per_s": wl.bls * D / sec}
@@ -547,10 +556,15 @@ def run_micro(args):
                 "ms": sec * 1e3, "tflops_causal": tf, "frac_tensor": tf / peaks["bf16_tflops"],
                 "peak_source": kind + " bf16_tflops"}
     if args.micro == "attn":
-        sec, gb = attn_case(args.B, args.H, args.d, args.L, args.iters, dev)
-        return {"micro": "decode_attn_g4", "B": args.B, "H": args.H, "d": args.d, "L": args.L,
-                "ms": sec * 1e3, "gbs": gb, "frac_hbm": gb / peaks["hbm_gbs"],
-                "peak_source": kind + " hbm_gbs"}
+        sec, gb = attn_case(args.B, args.H, args.d, args.L, args.iters, dev, topk=args.topk)
+        res = {"micro": "decode_attn_topk_g4" if 0 < args.topk < 100 else "decode_attn_g4",
+               "B": args.B, "H": args.H, "d": args.d, "L": args.L,
+               "ms": sec * 1e3, "gbs": gb, "frac_hbm": gb / peaks["hbm_gbs"],
+               "peak_source": kind + " hbm_gbs"}
+        if 0 < args.topk < 100:
+            dsec, _ = attn_case(args.B, args.H, args.d, args.L, args.iters, dev)
+            res.update({"keep_pct": args.topk, "dense_ms": dsec * 1e3, "speedup": dsec / sec})
+        return res
     # OPT-175B single-layer sweep: dequant-GEMM at bls in {32,144,256,512} for
     # the four projection shapes, decode attention at bls 144 for three contexts
     h1, H, h2 = synth.OPT175B_H1, synth.OPT175B_H, synth.OPT175B_H2
@@ -628,6 +642,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gbs", type=int, default=0, help="--micro decode: override gbs")
     ap.add_argument("--k", type=int, default=0, help="--micro decode: override k")
+    ap.add_argument("--topk", type=int, default=0,
+                    help="--micro attn/decode: top-K sparse decode attention keeping this percent "
+                         "of the rows (0: dense)")
     ap.add_argument("--micro", choices=["gemm", "attn", "prefill", "sweep175b", "decode"], default=None,
                     help="time one kernel shape (or the OPT-175B layer sweep) instead")
     ap.add_argument("--M", type=int, default=4096)

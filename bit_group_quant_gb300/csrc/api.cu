@@ -265,7 +265,7 @@ const char* fg_status_str(fg_status s) {
 
 const char* fg_last_error(void) { return g_err; }
 
-int32_t fg_version(void) { return (2 << 16) | 0; }
+int32_t fg_version(void) { return (3 << 16) | 0; }
 
 fg_status fg_check(fg_stream stream) {
     cudaError_t e = cudaStreamSynchronize(S(stream));
@@ -447,8 +447,37 @@ fg_status fg_decode_attn_g4(const fg_f16* qkv, int64_t qkv_ld, const fg_kv4* cac
                "decode_attn_g4: qkv and out must be 16-byte aligned");
     FG_REQUIRE((reinterpret_cast<uintptr_t>(pad) & 3u) == 0, FG_ERR_ALIGN,
                "decode_attn_g4: pad must be 4-byte aligned");
-    return fg::launch_decode_attn(H(qkv), qkv_ld, cache, pos, pad, fuse_append, Hm(out),
-                                  S(stream));
+    return fg::launch_decode_attn(H(qkv), qkv_ld, cache, pos, pad, fuse_append, 0, nullptr,
+                                  Hm(out), S(stream));
+}
+
+fg_status fg_decode_attn_topk_g4(const fg_f16* qkv, int64_t qkv_ld, const fg_kv4* cache,
+                                 int32_t pos, const int32_t* pad, int32_t keep_pct,
+                                 int32_t fuse_append, fg_f16* out, int32_t* sel_out,
+                                 fg_stream stream) {
+    fg_status s = check_kv(cache, "decode_attn_topk_g4");
+    if (s != FG_OK) return s;
+    FG_REQUIRE(qkv && out, FG_ERR_NULL, "decode_attn_topk_g4: null qkv or out");
+    const int64_t h1 = static_cast<int64_t>(cache->H) * cache->d;
+    FG_REQUIRE(qkv_ld >= 3 * h1 && qkv_ld % 8 == 0, FG_ERR_SHAPE,
+               "decode_attn_topk_g4: qkv_ld %lld must be >= 3*h1 and a multiple of 8", (long long)qkv_ld);
+    FG_REQUIRE(pos >= 0 && pos < cache->cap, FG_ERR_SHAPE,
+               "decode_attn_topk_g4: pos %d outside [0, %d)", pos, cache->cap);
+    FG_REQUIRE(keep_pct >= 1 && keep_pct <= 100, FG_ERR_SHAPE,
+               "decode_attn_topk_g4: keep_pct %d outside [1, 100]", keep_pct);
+    FG_REQUIRE(cache->cap <= 50000, FG_ERR_UNSUPPORTED, "decode_attn_topk_g4: cap %d > 50000", cache->cap);
+    FG_REQUIRE(fg::aligned16(qkv) && fg::aligned16(out), FG_ERR_ALIGN,
+               "decode_attn_topk_g4: qkv and out must be 16-byte aligned");
+    FG_REQUIRE((reinterpret_cast<uintptr_t>(pad) & 3u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(sel_out) & 3u) == 0,
+               FG_ERR_ALIGN, "decode_attn_topk_g4: pad and sel_out must be 4-byte aligned");
+    return fg::launch_decode_attn(H(qkv), qkv_ld, cache, pos, pad, fuse_append, keep_pct, sel_out,
+                                  Hm(out), S(stream));
+}
+
+int32_t fg_topk_count(int32_t n, int32_t keep_pct) {
+    if (n < 0 || keep_pct < 1 || keep_pct > 100) return -1;
+    return static_cast<int32_t>((static_cast<int64_t>(n) * keep_pct + 99) / 100);
 }
 
 fg_status fg_prefill_attn(const fg_f16* qkv, int32_t B, int32_t s_len, int32_t Hh, int32_t d,
@@ -495,6 +524,8 @@ fg_status fg_layer_step(const fg_layer* w, const fg_kv4* cache, const fg_f16* x_
                "layer_step: x_in and x_out must be 16-byte aligned");
     FG_REQUIRE(p.gbs > 0 && p.k > 0 && p.order >= 0 && p.order <= 2, FG_ERR_SHAPE,
                "layer_step: bad policy");
+    FG_REQUIRE(p.topk_pct >= 0 && p.topk_pct <= 100, FG_ERR_SHAPE,
+               "layer_step: topk_pct %d outside [0, 100]", p.topk_pct);
     const int32_t bls = p.gbs * p.k;
     FG_REQUIRE(cache->B == bls, FG_ERR_SHAPE, "layer_step: cache holds %d sequences, bls = %d",
                cache->B, bls);
@@ -547,7 +578,7 @@ fg_status fg_layer_step(const fg_layer* w, const fg_kv4* cache, const fg_f16* x_
             FG_RUN(fg::launch_prefill_attn(qkv, nb, T, w->H, d, pb, attn, st));
             FG_RUN(fg::launch_kv_store(qkv, 3 * h1, nb, T, w->H, d, &c, 0, st));
         } else {
-            FG_RUN(fg::launch_decode_attn(qkv, 3 * h1, &c, pos, pb, 1, attn, st));
+            FG_RUN(fg::launch_decode_attn(qkv, 3 * h1, &c, pos, pb, 1, p.topk_pct, nullptr, attn, st));
         }
         FG_RUN(fg::launch_gemm_g4(attn, nr, &w->out, H(w->b_out), xin, FG_ACT_NONE, hh, L.gemm,
                                   L.gemm_bytes, st, rows));

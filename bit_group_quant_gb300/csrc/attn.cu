@@ -81,11 +81,295 @@ __device__ __forceinline__ uint32_t ldg32(const uint8_t* p) {
     return *reinterpret_cast<const uint32_t*>(p);
 }
 
-template <int D>
+// ---------------------------------------------------------------------------
+// Top-K sparse decode attention ("FlexGen 完全拆解", section on the paper's
+// further approximations): the scores of every cached key are computed, and
+// only the V rows of the keep_pct percent highest scores are loaded.  The
+// softmax keeps its full maximum and normaliser over all attended rows; rows
+// not kept add nothing.  ceil(L * keep_pct / 100) rows are kept, equal
+// scores lowest slot first.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ int topk_count(int L, int keep_pct) {
+    return static_cast<int>((static_cast<int64_t>(L) * keep_pct + 99) / 100);
+}
+
+// Order-preserving unsigned key of an fp32 score: a larger score has a larger
+// key, and -0 and +0 (canonicalised by the addition) share one key.
+__device__ __forceinline__ uint32_t score_key(float f) {
+    const uint32_t u = __float_as_uint(f + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Shared scratch of topk_select: two 256-bin histograms, 16 ints, and up to
+// kTkCand candidate keys.
+constexpr int kTkCand = 128;
+constexpr int kTkScratchBytes = 2 * 256 * 4 + 64 + kTkCand * 4;
+
+// Bin of a score in 256 equal bins over [mn, mx] (inv = 256 / (mx - mn)):
+// each step is monotone in s, so a higher bin holds only higher scores.
+__device__ __forceinline__ uint32_t tk_bin(float s, float mn, float inv) {
+    return static_cast<uint32_t>(min(max(static_cast<int>((s - mn) * inv), 0), 255));
+}
+
+// The ksel highest of the scores sc[0..L) (equal scores: lower index first)
+// as ascending indices sel[0..ksel); also returns this thread's part of the
+// softmax normaliser, sum exp(s_j - mx) over j = tid, tid + blockDim, ...
+// (the dense kernels' order), mx / mn the scores' maximum / minimum.
+// The cut is found on order-preserving keys of the scores.  Usually one
+// histogram of the scores over 256 equal bins of [mn, mx] (built in the same
+// loop as the normaliser) gives the bin holding the ksel-th highest score;
+// its scores (at most kTkCand) are ranked exactly by one warp.  Otherwise
+// (a crowded bin, or all scores equal) a radix selection finds the cut key
+// in four 8-bit digit passes over alternating histograms.  Then one pass in
+// index order keeps every key above the cut and the first `need` keys equal
+// to it: each warp owns a contiguous range of indices, counts its keys above
+// and equal to the cut, and writes its kept indices after those of the
+// warps before it.  Block-wide: every thread calls it; ends with a barrier.
+__device__ float topk_select(const float* sc, int L, int ksel, float mx, float mn, int* sel,
+                             uint8_t* scratch) {
+    constexpr int NW = kDecThreads / 32;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint32_t* hist = reinterpret_cast<uint32_t*>(scratch);
+    int* ws = reinterpret_cast<int*>(scratch + 2 * 256 * 4);
+    uint32_t* cand = reinterpret_cast<uint32_t*>(scratch + 2 * 256 * 4 + 64);
+    const bool all = ksel >= L;
+    const float inv = 256.0f / (mx - mn);
+    const bool binned = !all && mx > mn && inv < CUDART_INF_F;   // block-uniform
+    if (binned) {
+        for (int i = tid; i < 256; i += kDecThreads) hist[i] = 0u;
+        if (tid == 0) ws[2] = 0;
+        __syncthreads();
+    }
+    float lsum = 0.0f;
+    for (int j = tid; j < L; j += kDecThreads) {
+        const float sj = sc[j];
+        lsum += expf(sj - mx);
+        if (binned) atomicAdd(&hist[tk_bin(sj, mn, inv)], 1u);
+    }
+    if (all) {
+        for (int j = tid; j < L; j += kDecThreads) sel[j] = j;
+        __syncthreads();
+        return lsum;
+    }
+    // the highest digit d of hc with #(above d) < need <= #(d and above):
+    // ws[0] = d, ws[1] = #(above d); warp 0 scans, lane l holding bins
+    // 255 - 8l .. 248 - 8l
+    auto scan = [&](const uint32_t* hc, uint32_t need) {
+        uint32_t c[8], cnt = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            c[i] = hc[255 - 8 * lane - i];
+            cnt += c[i];
+        }
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const uint32_t excl = incl - cnt;
+        if (excl < need && need <= incl) {   // exactly one lane
+            uint32_t acc = excl;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (acc + c[i] >= need) {
+                    ws[0] = 255 - 8 * lane - i;
+                    ws[1] = static_cast<int>(acc);
+                    break;
+                }
+                acc += c[i];
+            }
+        }
+    };
+    uint32_t prefix = 0u, need = static_cast<uint32_t>(ksel);
+    bool resolved = false;
+    if (binned) {
+        __syncthreads();
+        if (warp == 0) scan(hist, need);
+        __syncthreads();
+        const uint32_t bstar = static_cast<uint32_t>(ws[0]);
+        uint32_t need_b = need - static_cast<uint32_t>(ws[1]);   // kept from the cut bin
+        for (int j = tid; j < L; j += kDecThreads) {
+            const float sj = sc[j];
+            if (tk_bin(sj, mn, inv) == bstar) {
+                const int at = atomicAdd(&ws[2], 1);
+                if (at < kTkCand) cand[at] = score_key(sj);
+            }
+        }
+        __syncthreads();
+        const int nc = ws[2];
+        if (nc <= kTkCand) {
+            // the need-th highest candidate key T and how many exceed it
+            if (warp == 0) {
+                for (int i = lane; i < nc; i += 32) {
+                    const uint32_t ki = cand[i];
+                    uint32_t gt = 0u, ge = 0u;
+                    for (int m = 0; m < nc; ++m) {
+                        const uint32_t km = cand[m];
+                        gt += km > ki;
+                        ge += km >= ki;
+                    }
+                    if (gt < need_b && need_b <= ge) {   // lanes holding T agree
+                        ws[3] = static_cast<int>(ki);
+                        ws[4] = static_cast<int>(gt);
+                    }
+                }
+            }
+            __syncthreads();
+            prefix = static_cast<uint32_t>(ws[3]);
+            need = need_b - static_cast<uint32_t>(ws[4]);
+            resolved = true;
+        }
+    }
+    if (!resolved) {
+        for (int i = tid; i < 512; i += kDecThreads) hist[i] = 0u;
+        __syncthreads();
+        uint32_t pmask = 0u;
+#pragma unroll 1
+        for (int pass = 0; pass < 4; ++pass) {
+            const int shift = 24 - 8 * pass;
+            uint32_t* hc = hist + 256 * (pass & 1);
+            uint32_t* hn = hist + 256 * ((pass + 1) & 1);   // read last in pass - 1: free
+            for (int i = tid; i < 256; i += kDecThreads) hn[i] = 0u;
+            for (int j = tid; j < L; j += kDecThreads) {
+                const uint32_t k = score_key(sc[j]);
+                if ((k & pmask) == prefix) atomicAdd(&hc[(k >> shift) & 255u], 1u);
+            }
+            __syncthreads();
+            if (warp == 0) scan(hc, need);
+            __syncthreads();
+            // ws is rewritten only after the next pass's first barrier
+            prefix |= static_cast<uint32_t>(ws[0]) << shift;
+            pmask |= 0xFFu << shift;
+            need -= static_cast<uint32_t>(ws[1]);
+        }
+    }
+    // prefix: the key of the ksel-th highest score; need (>= 1) of the keys
+    // equal to it are kept, lowest index first.  Warp w owns [lo, hi).
+    const int per = (((L + NW - 1) / NW) + 31) & ~31;
+    const int lo = min(warp * per, L), hi = min(lo + per, L);
+    const uint32_t lt = (1u << lane) - 1u;
+    int gt_n = 0, eq_n = 0;
+    for (int c0 = lo; c0 < hi; c0 += 32) {
+        const int j = c0 + lane;
+        const uint32_t k = j < hi ? score_key(sc[j]) : 0u;
+        gt_n += __popc(__ballot_sync(0xffffffffu, j < hi && k > prefix));
+        eq_n += __popc(__ballot_sync(0xffffffffu, j < hi && k == prefix));
+    }
+    if (lane == 0) {
+        ws[5 + warp] = gt_n;
+        ws[5 + NW + warp] = eq_n;
+    }
+    __syncthreads();
+    int at = 0, eq_seen = 0;   // kept indices and equal keys of the warps before
+    for (int w = 0; w < warp; ++w) {
+        const int e = ws[5 + NW + w];
+        const int take_eq = min(e, max(static_cast<int>(need) - eq_seen, 0));
+        at += ws[5 + w] + take_eq;
+        eq_seen += e;
+    }
+    for (int c0 = lo; c0 < hi; c0 += 32) {
+        const int j = c0 + lane;
+        const uint32_t k = j < hi ? score_key(sc[j]) : 0u;
+        const bool eq = j < hi && k == prefix;
+        const unsigned beq = __ballot_sync(0xffffffffu, eq);
+        const bool take = (j < hi && k > prefix) ||
+                          (eq && static_cast<uint32_t>(eq_seen + __popc(beq & lt)) < need);
+        const unsigned bt = __ballot_sync(0xffffffffu, take);
+        if (take) sel[at + __popc(bt & lt)] = j;
+        at += __popc(bt);
+        eq_seen += __popc(beq);
+    }
+    __syncthreads();
+    return lsum;
+}
+
+// Pass 2 (the V sums) over nv keys read straight from global memory: key u
+// of the pass is cache row row0 + slot(u), slot(u) = u (dense) or sel[u]
+// (top-K, ascending), with weight p = sc[slot(u)] (dense: sc holds the
+// weights) or exp(sc[slot(u)] - mx) (top-K: sc holds the scores).  MMA e (nibble e of every
+// code word) has rows = dims (row g: word g, row g+8: word 8+g) and k = 16
+// keys paired in registers; B column n = g holds p * s_g (fp16) for group g.
+template <int D, bool TOPK>
+__device__ __forceinline__ void v_pass_global(const float* sc, float mx, const int* sel, int nv,
+                                              const uint8_t* v_codes, const float* v_meta,
+                                              int64_t row0, int warp, int g, int t,
+                                              float (&accv)[8][4], float& s_pm) {
+    constexpr int G = D / 64, RB = D / 2, NWARP = kDecThreads / 32;
+    const bool gown = g < G;
+    const int ntile = (nv + 15) >> 4;
+    for (int kt = warp; kt < ntile; kt += NWARP) {
+        const int j0 = kt * 16;
+        const int keys[4] = {j0 + 2 * t, j0 + 2 * t + 1, j0 + 2 * t + 8, j0 + 2 * t + 9};
+        int slot[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int uu = min(keys[u], nv - 1);
+            slot[u] = TOPK ? sel[uu] : uu;
+        }
+        uint32_t bw[2] = {0u, 0u};
+        {
+            float pp[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const bool ok = keys[u] < nv;
+                const float p = ok ? (TOPK ? expf(sc[slot[u]] - mx) : sc[slot[u]]) : 0.0f;
+                float pv = 0.0f;
+                if (gown && ok) {
+                    const float2 m = *reinterpret_cast<const float2*>(
+                        v_meta + ((row0 + slot[u]) * G + g) * 2);
+                    pv = p * m.y;
+                    s_pm += p * m.x;
+                }
+                pp[u] = pv;
+            }
+            bw[0] = pack_h2(pp[0], pp[1]);
+            bw[1] = pack_h2(pp[2], pp[3]);
+        }
+        // code words: word g (dims 8g..8g+7) and, for D = 128, word 8+g
+        uint32_t w0[4], w1[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint8_t* r = v_codes + (row0 + slot[u]) * RB;
+            w0[u] = ldg32(r + 4 * g);
+            w1[u] = (D == 128) ? ldg32(r + 32 + 4 * g) : 0u;
+        }
+        // (key pair, word) -> PRMT so each 16-bit half holds one key's nibbles
+        const uint32_t lo0 = __byte_perm(w0[0], w0[1], 0x5410), hi0 = __byte_perm(w0[0], w0[1], 0x7632);
+        const uint32_t lo2 = __byte_perm(w0[2], w0[3], 0x5410), hi2 = __byte_perm(w0[2], w0[3], 0x7632);
+        const uint32_t lo1 = __byte_perm(w1[0], w1[1], 0x5410), hi1 = __byte_perm(w1[0], w1[1], 0x7632);
+        const uint32_t lo3 = __byte_perm(w1[2], w1[3], 0x5410), hi3 = __byte_perm(w1[2], w1[3], 0x7632);
+        const uint32_t lo0s = lo0 >> 8, hi0s = hi0 >> 8, lo1s = lo1 >> 8, hi1s = hi1 >> 8;
+        const uint32_t lo2s = lo2 >> 8, hi2s = hi2 >> 8, lo3s = lo3 >> 8, hi3s = hi3 >> 8;
+        __syncwarp();   // mma.sync is .aligned: reconverge after the per-key loads above
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int p = e & 3;   // MMA e: codes k_e c 2^-24, k_e = 16 for odd e
+            const uint32_t a0 = e < 4 ? enc_pair(lo0, lo0s, p) : enc_pair(hi0, hi0s, p);
+            const uint32_t a2 = e < 4 ? enc_pair(lo2, lo2s, p) : enc_pair(hi2, hi2s, p);
+            const uint32_t a1 = (D == 128) ? (e < 4 ? enc_pair(lo1, lo1s, p) : enc_pair(hi1, hi1s, p)) : 0u;
+            const uint32_t a3 = (D == 128) ? (e < 4 ? enc_pair(lo3, lo3s, p) : enc_pair(hi3, hi3s, p)) : 0u;
+            mma16816(accv[e], a0, a1, a2, a3, bw[0], bw[1]);
+        }
+    }
+}
+
+// Kept slots of one (sequence, head) to sel_out[0..kmax): p0 + sel[r] for
+// r < nv, -1 after.
+__device__ __forceinline__ void write_kept(int32_t* dst, const int* sel, int nv, int kmax, int p0) {
+    for (int r = threadIdx.x; r < kmax; r += kDecThreads) dst[r] = r < nv ? p0 + sel[r] : -1;
+}
+
+// TOPK: top-K sparse attention (keep_pct percent of the rows, the kept slots
+// optionally written to sel_out [B][H][kmax]); dynamic shared memory holds
+// the L scores, then (TOPK) kmax kept indices, the histogram and scratch.
+template <int D, bool TOPK>
 __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
     const __half* __restrict__ qkv, int64_t ld, int32_t H, int32_t cap, int32_t pos,
     const int32_t* __restrict__ pad, int32_t fuse_append, uint8_t* k_codes, uint8_t* v_codes,
-    float* k_meta, float* v_meta, __half* __restrict__ out) {
+    float* k_meta, float* v_meta, __half* __restrict__ out, int32_t keep_pct, int32_t kmax,
+    int32_t* __restrict__ sel_out) {
     constexpr int G = D / 64;            // groups per head row
     constexpr int RB = D / 2;            // code bytes per row
     constexpr int WPT = D / 32;          // code words per lane per row in pass 1
@@ -94,6 +378,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
     extern __shared__ float dsm[];
     __shared__ float qsum[G];
     __shared__ float red[NWARP];
+    __shared__ float red_min[NWARP];
     __shared__ float part[NWARP][D];
     __shared__ float part_s[NWARP][2][2];   // per warp, per group: sum p m, sum p'
 
@@ -183,7 +468,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
     const int ntile = (L + 15) >> 4;
 
     // ---------------- pass 1: scores
-    float lmax = -CUDART_INF_F;
+    float lmax = -CUDART_INF_F, lmin = CUDART_INF_F;   // lmin: TOPK only
     for (int kt = warp; kt < ntile; kt += NWARP) {
         const int ja = min(kt * 16 + g, L - 1), jb = min(kt * 16 + g + 8, L - 1);
         const uint8_t* ra = k_codes + (row0 + ja) * RB + t * (WPT * 4);
@@ -236,22 +521,42 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
                     const float s = dot * attn_scale;
                     sc[j] = s;
                     lmax = fmaxf(lmax, s);
+                    if (TOPK) lmin = fminf(lmin, s);
                 }
             }
         }
     }
     lmax = warp_max(lmax);
     if (lane == 0) red[warp] = lmax;
+    if (TOPK) {
+        lmin = -warp_max(-lmin);
+        if (lane == 0) red_min[warp] = lmin;
+    }
     __syncthreads();
-    float mx = red[0];
+    float mx = red[0], mn = TOPK ? red_min[0] : 0.0f;
 #pragma unroll
-    for (int i = 1; i < NWARP; ++i) mx = fmaxf(mx, red[i]);
+    for (int i = 1; i < NWARP; ++i) {
+        mx = fmaxf(mx, red[i]);
+        if (TOPK) mn = fminf(mn, red_min[i]);
+    }
     __syncthreads();
+    int nv = L;            // keys of pass 2
+    int* sel = nullptr;    // TOPK: their slots (offsets from p0), ascending
     float lsum = 0.0f;
-    for (int j = threadIdx.x; j < L; j += kDecThreads) {
-        const float p = expf(sc[j] - mx);
-        sc[j] = p;
-        lsum += p;
+    if constexpr (TOPK) {
+        // the scores stay in sc (pass 2 takes exp of the kept ones)
+        const int Lp = (pos + 4) & ~3;   // the scores' space, for the largest L
+        sel = reinterpret_cast<int*>(dsm + Lp);
+        nv = topk_count(L, keep_pct);
+        lsum = topk_select(sc, L, nv, mx, mn, sel,
+                           reinterpret_cast<uint8_t*>(sel + ((kmax + 3) & ~3)));
+        if (sel_out) write_kept(sel_out + (static_cast<int64_t>(b) * H + h) * kmax, sel, nv, kmax, p0);
+    } else {
+        for (int j = threadIdx.x; j < L; j += kDecThreads) {
+            const float p = expf(sc[j] - mx);
+            sc[j] = p;
+            lsum += p;
+        }
     }
     lsum = warp_sum(lsum);
     if (lane == 0) red[warp] = lsum;
@@ -260,64 +565,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
 #pragma unroll
     for (int i = 0; i < NWARP; ++i) l += red[i];
 
-    // ---------------- pass 2: V.  MMA e (nibble e of every code word) has rows
-    // = dims (row g: word g, row g+8: word 8+g) and k = 16 keys paired in
-    // registers; B column n = g holds p_j * s_{j,g} (fp16) for group g.
+    // ---------------- pass 2: V (all L rows, or the kept ones)
     float accv[8][4];
 #pragma unroll
     for (int e = 0; e < 8; ++e) accv[e][0] = accv[e][1] = accv[e][2] = accv[e][3] = 0.0f;
     float s_pm = 0.0f;   // this lane's keys: sum p * min (group g)
     const bool gown = g < G;
-    for (int kt = warp; kt < ntile; kt += NWARP) {
-        const int j0 = kt * 16;
-        int keys[4] = {j0 + 2 * t, j0 + 2 * t + 1, j0 + 2 * t + 8, j0 + 2 * t + 9};
-        uint32_t bw[2] = {0u, 0u};
-        {
-            float pp[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const bool ok = keys[u] < L;
-                const float p = ok ? sc[keys[u]] : 0.0f;
-                float pv = 0.0f;
-                if (gown && ok) {
-                    const float2 m = *reinterpret_cast<const float2*>(
-                        v_meta + ((row0 + keys[u]) * G + g) * 2);
-                    pv = p * m.y;
-                    s_pm += p * m.x;
-                }
-                pp[u] = pv;
-            }
-            bw[0] = pack_h2(pp[0], pp[1]);
-            bw[1] = pack_h2(pp[2], pp[3]);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) keys[u] = min(keys[u], L - 1);
-        // code words: word g (dims 8g..8g+7) and, for D = 128, word 8+g
-        uint32_t w0[4], w1[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const uint8_t* r = v_codes + (row0 + keys[u]) * RB;
-            w0[u] = ldg32(r + 4 * g);
-            w1[u] = (D == 128) ? ldg32(r + 32 + 4 * g) : 0u;
-        }
-        // (key pair, word) -> PRMT so each 16-bit half holds one key's nibbles
-        const uint32_t lo0 = __byte_perm(w0[0], w0[1], 0x5410), hi0 = __byte_perm(w0[0], w0[1], 0x7632);
-        const uint32_t lo2 = __byte_perm(w0[2], w0[3], 0x5410), hi2 = __byte_perm(w0[2], w0[3], 0x7632);
-        const uint32_t lo1 = __byte_perm(w1[0], w1[1], 0x5410), hi1 = __byte_perm(w1[0], w1[1], 0x7632);
-        const uint32_t lo3 = __byte_perm(w1[2], w1[3], 0x5410), hi3 = __byte_perm(w1[2], w1[3], 0x7632);
-        const uint32_t lo0s = lo0 >> 8, hi0s = hi0 >> 8, lo1s = lo1 >> 8, hi1s = hi1 >> 8;
-        const uint32_t lo2s = lo2 >> 8, hi2s = hi2 >> 8, lo3s = lo3 >> 8, hi3s = hi3 >> 8;
-        __syncwarp();   // mma.sync is .aligned: reconverge after the per-key loads above
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int p = e & 3;   // MMA e: codes k_e c 2^-24, k_e = 16 for odd e
-            const uint32_t a0 = e < 4 ? enc_pair(lo0, lo0s, p) : enc_pair(hi0, hi0s, p);
-            const uint32_t a2 = e < 4 ? enc_pair(lo2, lo2s, p) : enc_pair(hi2, hi2s, p);
-            const uint32_t a1 = (D == 128) ? (e < 4 ? enc_pair(lo1, lo1s, p) : enc_pair(hi1, hi1s, p)) : 0u;
-            const uint32_t a3 = (D == 128) ? (e < 4 ? enc_pair(lo3, lo3s, p) : enc_pair(hi3, hi3s, p)) : 0u;
-            mma16816(accv[e], a0, a1, a2, a3, bw[0], bw[1]);
-        }
-    }
+    v_pass_global<D, TOPK>(sc, mx, sel, nv, v_codes, v_meta, row0, warp, g, t, accv, s_pm);
     // group sums of this warp: reduce over the 4 lanes (g, t) of each group
 #pragma unroll
     for (int o = 1; o < 4; o <<= 1) s_pm += __shfl_xor_sync(0xffffffffu, s_pm, o);
@@ -367,17 +621,27 @@ constexpr int kRB128 = 64;         // code bytes per row (d = 128)
 constexpr int kMB128 = 16;         // (min, scale) bytes per row (2 groups)
 constexpr int kChunkBytes = kCKMax * (kRB128 + kMB128);   // codes, then meta
 
+// TOPK: top-K sparse attention.  Only the K chunks are staged; after pass 1
+// the idle ring holds the selection's histogram, scratch and kept indices
+// (after the scores instead when kmax is too large for it), and pass 2
+// gathers the kept V rows straight from global memory.
+__host__ __device__ constexpr bool topk_in_ring(int kmax) {
+    return kTkScratchBytes + 4 * ((kmax + 3) & ~3) <= kNB * kChunkBytes;
+}
+
+template <bool TOPK>
 __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_kernel(
     const __half* __restrict__ qkv, int64_t ld, int32_t H, int32_t cap, int32_t pos,
     const int32_t* __restrict__ pad, int32_t fuse_append, uint8_t* k_codes, uint8_t* v_codes,
     float* k_meta, float* v_meta, __half* __restrict__ out, int* status,
-    unsigned long long wait_ns) {
+    unsigned long long wait_ns, int32_t keep_pct, int32_t kmax, int32_t* __restrict__ sel_out) {
     constexpr int D = 128, G = 2, RB = kRB128, WPT = D / 32, NX = 2 * WPT;
     constexpr int NWARP = kDecThreads / 32;
     extern __shared__ __align__(128) uint8_t dyn[];
     __shared__ __align__(8) uint64_t full_bar[kNB];
     __shared__ float qsum[G];
     __shared__ float red[NWARP];
+    __shared__ float red_min[NWARP];
     __shared__ float part[NWARP][D];
     __shared__ float part_s[NWARP][2][2];
     __shared__ int fail_sh;
@@ -389,7 +653,7 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     // chunks of kCK keys; a remainder of <= 16 keys joins the last full chunk
     int nK = (L + kCK - 1) / kCK;
     if (nK > 1 && L - (nK - 1) * kCK <= 16) --nK;
-    const int nseq = 2 * nK;
+    const int nseq = TOPK ? nK : 2 * nK;   // K chunks, then (dense) V chunks
     auto chunk_n = [&](int c) { return c == nK - 1 ? L - c * kCK : kCK; };
     const int64_t h1 = static_cast<int64_t>(H) * D;
     const int64_t rowb = (static_cast<int64_t>(b) * H + h) * cap;  // cache row of slot 0
@@ -503,7 +767,7 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     const float Q0 = qsum[0], Q1 = qsum[1];
 
     // ---------------- pass 1: scores
-    float lmax = -CUDART_INF_F;
+    float lmax = -CUDART_INF_F, lmin = CUDART_INF_F;   // lmin: TOPK only
     for (int c = 0; c < nK; ++c) {
         const bool ok = wait_chunk(c);
         const uint8_t* buf = dyn + (c % kNB) * kChunkBytes;
@@ -543,6 +807,7 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
                         const float s = dot * attn_scale;
                         sc[r0 + jl] = s;
                         lmax = fmaxf(lmax, s);
+                        if (TOPK) lmin = fminf(lmin, s);
                     }
                 }
             }
@@ -556,13 +821,33 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     }
     lmax = warp_max(lmax);
     if (lane == 0) red[warp] = lmax;
+    if (TOPK) {
+        lmin = -warp_max(-lmin);
+        if (lane == 0) red_min[warp] = lmin;
+    }
     __syncthreads();
-    float mx = red[0];
+    float mx = red[0], mn = TOPK ? red_min[0] : 0.0f;
 #pragma unroll
-    for (int i = 1; i < NWARP; ++i) mx = fmaxf(mx, red[i]);
+    for (int i = 1; i < NWARP; ++i) {
+        mx = fmaxf(mx, red[i]);
+        if (TOPK) mn = fminf(mn, red_min[i]);
+    }
     __syncthreads();
+    int nv = L;            // TOPK: kept keys
+    int* sel = nullptr;    // TOPK: their slots (offsets from p0), ascending
     float lsum = 0.0f;
-    if (!failed) {
+    if constexpr (TOPK) {
+        if (!failed) {     // block-uniform; no chunk is in flight after a clean pass 1
+            // scratch, then the kept list: in the idle ring, or after the scores
+            uint8_t* x = topk_in_ring(kmax) ? dyn
+                                            : dyn + kNB * kChunkBytes + 4 * ((pos + 4) & ~3);
+            sel = reinterpret_cast<int*>(x + kTkScratchBytes);
+            nv = topk_count(L, keep_pct);
+            lsum = topk_select(sc, L, nv, mx, mn, sel, x);   // the scores stay in sc
+            if (sel_out) write_kept(sel_out + (static_cast<int64_t>(b) * H + h) * kmax, sel, nv, kmax, p0);
+        }
+    }
+    if (!TOPK && !failed) {
         for (int j = threadIdx.x; j < L; j += kDecThreads) {
             const float p = expf(sc[j] - mx);
             sc[j] = p;
@@ -582,7 +867,8 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     for (int e = 0; e < 8; ++e) accv[e][0] = accv[e][1] = accv[e][2] = accv[e][3] = 0.0f;
     float s_pm = 0.0f;   // this lane's keys: sum p * min (group g)
     const bool gown = g < G;
-    for (int c = 0; c < nK && !failed; ++c) {
+    if (TOPK && !failed) v_pass_global<D, true>(sc, mx, sel, nv, v_codes, v_meta, row0, warp, g, t, accv, s_pm);
+    for (int c = 0; c < nK && !failed && !TOPK; ++c) {
         const int seq = nK + c;
         const bool ok = wait_chunk(seq);
         const uint8_t* buf = dyn + (seq % kNB) * kChunkBytes;
@@ -881,47 +1167,72 @@ __global__ void __launch_bounds__(128) prefill_attn_fa_kernel(const __half* __re
     }
 }
 
-template <int D>
+// Dynamic shared memory a block may use (227 KB less the kernels' static arrays).
+constexpr size_t kMaxDynSmem = 220 * 1024;
+
+// Rows kept by top-K attention over L rows (host copy of topk_count).
+int topk_count_host(int L, int keep_pct) {
+    return static_cast<int>((static_cast<int64_t>(L) * keep_pct + 99) / 100);
+}
+
+// Algorithmic bytes of one decode-attention launch: per (b, h) the L packed
+// K rows and the V rows summed (all L, or the kept ones), codes + fp32 meta;
+// the new k, v written back; q/k/v read and the output written.
+double decode_attn_bytes(int D, double bh, int L, int nv, bool fuse_append) {
+    const double row = D / 2 + (D / 64) * 8.0;
+    return bh * ((static_cast<double>(L) + nv) * row + (fuse_append ? 2.0 * row : 0.0) + 3.0 * D * 2 + D * 2);
+}
+
+template <int D, bool TOPK>
 fg_status launch_decode_t(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
-                          const int32_t* pad, int32_t fuse_append, __half* out, cudaStream_t st) {
+                          const int32_t* pad, int32_t fuse_append, int32_t keep_pct, int32_t kmax,
+                          int32_t* sel_out, __half* out, cudaStream_t st) {
     const int L = pos + 1;
-    const size_t smem = sizeof(float) * ((L + 3) & ~3);
-    auto kern = decode_attn_kernel<D>;
+    size_t smem = sizeof(float) * ((L + 3) & ~3);
+    if (TOPK) smem += 4 * static_cast<size_t>((kmax + 3) & ~3) + kTkScratchBytes;
+    if (smem > kMaxDynSmem)
+        return fg::set_error(FG_ERR_UNSUPPORTED, "decode_attn: context %d at keep %d%% needs %zu B of shared memory",
+                             L, TOPK ? keep_pct : 100, smem);
+    auto kern = decode_attn_kernel<D, TOPK>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return fg::cuda_error(e, "decode_attn smem attribute");
     }
     dim3 grid(c->H, c->B);
-    // algorithmic traffic: L packed K and V rows (codes + fp32 meta) per (b, h),
-    // the new k, v written back, q/k/v read and the output written
-    const double row = D / 2 + (D / 64) * 8.0;
     const double bh = static_cast<double>(c->B) * c->H;
     fg::TraceScope ts(FG_TRACE_ATTN_DECODE, st, 4.0 * bh * L * D,
-                      bh * (2.0 * L * row + (fuse_append ? 2.0 * row : 0.0) + 3.0 * D * 2 + D * 2));
+                      decode_attn_bytes(D, bh, L, TOPK ? kmax : L, fuse_append != 0));
     kern<<<grid, kDecThreads, smem, st>>>(qkv, ld, c->H, c->cap, pos, pad, fuse_append,
-                                          c->k_codes, c->v_codes, c->k_meta, c->v_meta, out);
+                                          c->k_codes, c->v_codes, c->k_meta, c->v_meta, out,
+                                          keep_pct, kmax, sel_out);
     return fg::cuda_error(cudaGetLastError(), "decode_attn launch");
 }
 
+template <bool TOPK>
 fg_status launch_decode_staged(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
-                               const int32_t* pad, int32_t fuse_append, __half* out,
-                               cudaStream_t st) {
+                               const int32_t* pad, int32_t fuse_append, int32_t keep_pct,
+                               int32_t kmax, int32_t* sel_out, __half* out, cudaStream_t st) {
     constexpr int D = 128;
     const int L = pos + 1;
-    const size_t smem = static_cast<size_t>(kNB) * kChunkBytes + sizeof(float) * ((L + 3) & ~3);
-    auto kern = decode_attn_staged_kernel;
+    size_t smem = static_cast<size_t>(kNB) * kChunkBytes + sizeof(float) * ((L + 3) & ~3);
+    if (TOPK && !topk_in_ring(kmax))
+        smem += 4 * static_cast<size_t>((kmax + 3) & ~3) + kTkScratchBytes;
+    if (smem > kMaxDynSmem)
+        return fg::set_error(FG_ERR_UNSUPPORTED, "decode_attn: context %d at keep %d%% needs %zu B of shared memory",
+                             L, TOPK ? keep_pct : 100, smem);
+    auto kern = decode_attn_staged_kernel<TOPK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return fg::cuda_error(e, "decode_attn smem attribute");
     dim3 grid(c->H, c->B);
-    const double row = D / 2 + (D / 64) * 8.0;
     const double bh = static_cast<double>(c->B) * c->H;
     fg::TraceScope ts(FG_TRACE_ATTN_DECODE, st, 4.0 * bh * L * D,
-                      bh * (2.0 * L * row + (fuse_append ? 2.0 * row : 0.0) + 3.0 * D * 2 + D * 2));
+                      decode_attn_bytes(D, bh, L, TOPK ? kmax : L, fuse_append != 0));
     kern<<<grid, kDecThreads, smem, st>>>(qkv, ld, c->H, c->cap, pos, pad, fuse_append,
                                           c->k_codes, c->v_codes, c->k_meta, c->v_meta, out,
-                                          fg::device_status_ptr(), fg::wait_limit_ns());
+                                          fg::device_status_ptr(), fg::wait_limit_ns(), keep_pct,
+                                          kmax, sel_out);
     return fg::cuda_error(cudaGetLastError(), "decode_attn launch");
 }
 
@@ -930,11 +1241,22 @@ fg_status launch_decode_staged(const __half* qkv, int64_t ld, const fg_kv4* c, i
 namespace fg {
 
 fg_status launch_decode_attn(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
-                             const int32_t* pad, int32_t fuse_append, __half* out,
-                             cudaStream_t st) {
+                             const int32_t* pad, int32_t fuse_append, int32_t keep_pct,
+                             int32_t* sel_out, __half* out, cudaStream_t st) {
     if (c->B == 0) return FG_OK;
-    if (c->d == 64) return launch_decode_t<64>(qkv, ld, c, pos, pad, fuse_append, out, st);
-    return launch_decode_staged(qkv, ld, c, pos, pad, fuse_append, out, st);
+    // dense unless rows are dropped or the kept slots are asked for
+    const bool topk = sel_out != nullptr || (keep_pct > 0 && keep_pct < 100);
+    const int32_t pct = (keep_pct > 0 && keep_pct < 100) ? keep_pct : 100;
+    const int32_t kmax = topk ? topk_count_host(pos + 1, pct) : 0;
+    if (c->d == 64)
+        return topk ? launch_decode_t<64, true>(qkv, ld, c, pos, pad, fuse_append, pct, kmax, sel_out, out, st)
+                    : launch_decode_t<64, false>(qkv, ld, c, pos, pad, fuse_append, 0, 0, nullptr, out, st);
+    return topk ? launch_decode_staged<true>(qkv, ld, c, pos, pad, fuse_append, pct, kmax, sel_out, out, st)
+                : launch_decode_staged<false>(qkv, ld, c, pos, pad, fuse_append, 0, 0, nullptr, out, st);
+}
+
+int32_t decode_topk_kmax(int32_t pos, int32_t keep_pct) {
+    return topk_count_host(pos + 1, (keep_pct > 0 && keep_pct < 100) ? keep_pct : 100);
 }
 
 fg_status launch_prefill_attn(const __half* qkv, int32_t B, int32_t s, int32_t H, int32_t d,

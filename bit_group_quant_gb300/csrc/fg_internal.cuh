@@ -60,9 +60,13 @@ fg_status launch_embed(const int32_t* ids, int64_t ntok, int32_t T, int32_t pos0
                        const int32_t* pad, const __half* e_tok, const __half* e_pos, int32_t h1,
                        __half* y, cudaStream_t st);
 fg_status launch_argmax(const float* logits, int64_t B, int64_t V, int32_t* out, cudaStream_t st);
+// keep_pct 0 or 100 with sel_out NULL: dense attention; otherwise top-K
+// sparse attention keeping ceil(L * keep_pct / 100) rows (keep_pct 0 read as
+// 100), the kept slots written to sel_out [B][H][decode_topk_kmax] if given.
 fg_status launch_decode_attn(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
-                             const int32_t* pad, int32_t fuse_append, __half* out,
-                             cudaStream_t st);
+                             const int32_t* pad, int32_t fuse_append, int32_t keep_pct,
+                             int32_t* sel_out, __half* out, cudaStream_t st);
+int32_t decode_topk_kmax(int32_t pos, int32_t keep_pct);
 fg_status launch_prefill_attn(const __half* qkv, int32_t B, int32_t s, int32_t H, int32_t d,
                               const int32_t* pad, __half* out, cudaStream_t st);
 

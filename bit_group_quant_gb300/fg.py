@@ -29,7 +29,7 @@ EXPORTS = (
     "fg_gemm_f16_f32out", "fg_layernorm", "fg_embed", "fg_kv_append_g4",
     "fg_decode_attn_g4", "fg_prefill_attn", "fg_layer_workspace_bytes", "fg_layer_step",
     "fg_debug_set", "fg_trace_begin", "fg_trace_end", "fg_dequant_gemm_g4_noalloc",
-    "fg_argmax",
+    "fg_argmax", "fg_decode_attn_topk_g4", "fg_topk_count",
 )
 
 
@@ -52,7 +52,8 @@ class c_kv4(ctypes.Structure):
 
 
 class c_policy(ctypes.Structure):
-    _fields_ = [("gbs", ctypes.c_int32), ("k", ctypes.c_int32), ("order", ctypes.c_int32)]
+    _fields_ = [("gbs", ctypes.c_int32), ("k", ctypes.c_int32), ("order", ctypes.c_int32),
+                ("topk_pct", ctypes.c_int32)]
 
 
 class c_layer(ctypes.Structure):
@@ -107,6 +108,9 @@ def load(path: str = LIB_PATH):
             "fg_argmax": ([P, I64, I64, P, P], st),
             "fg_kv_append_g4": ([P, I64, ctypes.POINTER(c_kv4), I32, P], st),
             "fg_decode_attn_g4": ([P, I64, ctypes.POINTER(c_kv4), I32, P, I32, P, P], st),
+            "fg_decode_attn_topk_g4": ([P, I64, ctypes.POINTER(c_kv4), I32, P, I32, I32, P, P, P],
+                                       st),
+            "fg_topk_count": ([I32, I32], I32),
             "fg_prefill_attn": ([P, I32, I32, I32, I32, P, ctypes.POINTER(c_kv4), P, P], st),
             "fg_layer_workspace_bytes": ([ctypes.POINTER(c_layer), I32, I32, I32, c_policy], SZ),
             "fg_layer_step": ([ctypes.POINTER(c_layer), ctypes.POINTER(c_kv4), P, P, I32, I32,
@@ -352,6 +356,30 @@ def fg_decode_attn_g4(qkv, cache: KV4, pos, fuse_append=True, out=None, stream=N
                                  _pad(pad, cache.B), 1 if fuse_append else 0, _ptr(out),
                                  _stream(stream)))
     return out
+
+
+def fg_topk_count(n, keep_pct) -> int:
+    return int(load().fg_topk_count(int(n), int(keep_pct)))
+
+
+def fg_decode_attn_topk_g4(qkv, cache: KV4, pos, keep_pct, fuse_append=True, out=None,
+                           sel_out=None, stream=None, pad=None):
+    """sel_out: None, True (allocate [B][H][kmax] int32 and return it), or a
+    device int32 tensor of that shape.  Returns out, or (out, sel_out)."""
+    if out is None:
+        out = torch.empty((qkv.shape[0], cache.H * cache.d), dtype=torch.float16,
+                          device=qkv.device)
+    want = sel_out is not None
+    if sel_out is True:
+        kmax = fg_topk_count(pos + 1, keep_pct)
+        sel_out = torch.empty((cache.B, cache.H, max(kmax, 0)), dtype=torch.int32,
+                              device=qkv.device)
+    c = cache.c()
+    _ok(load().fg_decode_attn_topk_g4(_ptr(qkv), qkv.shape[1], ctypes.byref(c), int(pos),
+                                      _pad(pad, cache.B), int(keep_pct), 1 if fuse_append else 0,
+                                      _ptr(out), _ptr(sel_out) if want else None,
+                                      _stream(stream)))
+    return (out, sel_out) if want else out
 
 
 def fg_prefill_attn(qkv, B, s, H, d, cache: KV4 | None = None, out=None, stream=None, pad=None):

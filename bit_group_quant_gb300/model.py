@@ -81,7 +81,11 @@ def order_for(step: int, order: str) -> int:
 
 class LayerStack:
     """l decoder layers with their KV caches and one shared workspace for a
-    block of bls = gbs * k sequences."""
+    block of bls = gbs * k sequences.  topk_pct: 0 for dense decode
+    attention, 1..99 for top-K sparse decode attention keeping that percent
+    of the cached rows' V (the prefill stays dense)."""
+
+    topk_pct = 0
 
     def __init__(self, layers, gbs: int, k: int, cap: int, device="cuda"):
         self.layers = layers
@@ -99,7 +103,7 @@ class LayerStack:
         return self.gbs * self.k
 
     def policy(self, order_code: int) -> fg.c_policy:
-        return fg.c_policy(self.gbs, self.k, order_code)
+        return fg.c_policy(self.gbs, self.k, order_code, self.topk_pct)
 
     def workspace(self, phase, T, order_code):
         key = (phase, T, order_code != fg.FG_ORDER_BLOCK)

@@ -104,10 +104,14 @@ typedef struct fg_kv4 {
  * its K split from the block's row count (bls * T), so the batches and the
  * whole block sum each output in the same order. */
 enum { FG_ORDER_BLOCK = 0, FG_ORDER_BATCHES = 1, FG_ORDER_BATCHES_REV = 2 };
+/* topk_pct: 0 (or 100) for dense decode attention; 1..99 runs each decode
+ * step's attention as fg_decode_attn_topk_g4 at that percentage (the prefill
+ * stays dense).  (ABI 3.0 added this field.) */
 typedef struct fg_policy {
     int32_t gbs;
     int32_t k;
     int32_t order;
+    int32_t topk_pct;
 } fg_policy;
 
 /* One OPT decoder layer (pre-LayerNorm, ReLU FFN).  qkv: [3*h1][h1] with
@@ -260,6 +264,34 @@ fg_status fg_decode_attn_g4(const fg_f16* qkv, int64_t qkv_ld,
                             const fg_kv4* cache, int32_t pos,
                             const int32_t* pad, int32_t fuse_append,
                             fg_f16* out, fg_stream stream);
+
+/* Top-K sparse decode attention over the 4-bit cache ("FlexGen 完全拆解",
+ * section on the paper's further approximations: the scores of every cached
+ * key are computed, and only the V rows with the highest scores are loaded).
+ * For each sequence b and head h with n = pos + 1 - pad[b] attended slots:
+ * the scores s_j = q . k^_j / sqrt(d) and the full softmax weights
+ * p_j = exp(s_j - max s) / sum_all exp(s - max s) over all n slots, as in
+ * fg_decode_attn_g4; the kept set S = the fg_topk_count(n, keep_pct) slots
+ * with the highest fp32 scores (equal scores: lower slot first); and
+ * out = sum_{j in S} p_j v^_j -- rows outside S add nothing, the weights are
+ * not renormalised over S.  Only the V rows of S are read from memory.
+ * keep_pct in [1, 100]; 100 keeps every row and gives bit for bit the output
+ * of fg_decode_attn_g4.  sel_out: NULL, or device [B][H][kmax] int32 with
+ * kmax = fg_topk_count(pos + 1, keep_pct), receiving each (b, h)'s kept slots
+ * ascending, -1 after its own count.  Other arguments, layouts and fusion as
+ * for fg_decode_attn_g4.  Errors: FG_ERR_SHAPE for keep_pct outside [1, 100];
+ * FG_ERR_ALIGN if pad or sel_out is not 4-byte aligned; FG_ERR_UNSUPPORTED
+ * if the context's scores and kept list exceed a block's shared memory
+ * (about 27,000 slots at keep_pct 100). */
+fg_status fg_decode_attn_topk_g4(const fg_f16* qkv, int64_t qkv_ld,
+                                 const fg_kv4* cache, int32_t pos,
+                                 const int32_t* pad, int32_t keep_pct,
+                                 int32_t fuse_append, fg_f16* out,
+                                 int32_t* sel_out, fg_stream stream);
+
+/* Rows kept by top-K attention out of n: ceil(n * keep_pct / 100) (at least
+ * one for n >= 1).  Returns -1 for n < 0 or keep_pct outside [1, 100]. */
+int32_t fg_topk_count(int32_t n, int32_t keep_pct);
 
 /* Causal prefill attention for B sequences of s prompt tokens over the fp16
  * K, V straight from the QKV projection: out_i = sum_{pad[b]<=j<=i}

@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert fg.fg_version() >> 16 == 2
+    assert fg.fg_version() >> 16 == 3
     assert lib.fg_status_str(fg.FG_ERR_TIMEOUT) == b"device wait timed out"
 
 
@@ -66,6 +66,16 @@ def test_host_validation_rejects_without_launch(lib):
                                  None) == fg.FG_ERR_SHAPE               # pos == cap
     assert lib.fg_decode_attn_g4(P(0x5000), 384, ctypes.byref(kv), 7, P(0x7002), 1, P(0x6000),
                                  None) == fg.FG_ERR_ALIGN               # pad misaligned
+    for pct in (0, 101, -5):                                            # keep_pct outside [1, 100]
+        assert lib.fg_decode_attn_topk_g4(P(0x5000), 384, ctypes.byref(kv), 7, None, pct, 1,
+                                          P(0x6000), None, None) == fg.FG_ERR_SHAPE
+    assert lib.fg_decode_attn_topk_g4(P(0x5000), 384, ctypes.byref(kv), 7, None, 10, 1,
+                                      P(0x6000), P(0x7001), None) == fg.FG_ERR_ALIGN   # sel_out
+    assert lib.fg_decode_attn_topk_g4(P(0x5000), 384, ctypes.byref(kv), 8, None, 10, 1,
+                                      P(0x6000), None, None) == fg.FG_ERR_SHAPE        # pos == cap
+    for n, pct, want in [(513, 10, 52), (1, 10, 1), (10, 10, 1), (11, 10, 2), (7, 100, 7),
+                         (0, 10, 0), (5, 0, -1), (5, 101, -1), (-1, 10, -1)]:
+        assert lib.fg_topk_count(n, pct) == want
     assert lib.fg_kv_append_g4(P(0x5000), 100, ctypes.byref(kv), 0, None) == fg.FG_ERR_SHAPE
     assert lib.fg_layernorm(P(0x1000), 4, 100, 100, P(0x2000), P(0x3000), 1e-5, P(0x4000),
                             None) == fg.FG_ERR_SHAPE
@@ -102,6 +112,10 @@ def test_layer_step_validation(lib):
     st = lib.fg_layer_step(ctypes.byref(L), ctypes.byref(kv), P(0x5000), P(0x6000), 1, 1, 3,
                            None, pol, P(0x100000), 16, None)
     assert st == fg.FG_ERR_WORKSPACE
+    for bad in (-1, 101):
+        st = lib.fg_layer_step(ctypes.byref(L), ctypes.byref(kv), P(0x5000), P(0x6000), 1, 1, 3,
+                               None, fg.c_policy(2, 2, 0, bad), P(0x100000), 1 << 30, None)
+        assert st == fg.FG_ERR_SHAPE and b"topk_pct" in lib.fg_last_error()
     L.fc1 = q(h2 + 64, h1)
     st = lib.fg_layer_step(ctypes.byref(L), ctypes.byref(kv), P(0x5000), P(0x6000), 1, 1, 3,
                            None, pol, P(0x100000), 1 << 30, None)
