@@ -89,6 +89,8 @@ def _load():
                 "or_decode_attn_topk_g4": ([P, I64, P, P, P, P, I32, I32, I32, I32, I32, I32, P,
                                             I32, P, P, P], None),
                 "or_topk_count": ([I64, I32], I32),
+                "or_kv_store_prefill_f16": ([P, I32, I32, P, P, I32, I32, I32], None),
+                "or_decode_attn_f16": ([P, I64, P, P, I32, I32, I32, I32, I32, I32, P, P], None),
                 "or_argmax": ([P, I64, I64, P], None),
             }
             for name, (args, res) in sig.items():
@@ -303,6 +305,43 @@ def decode_attn_g4(qkv, cache: KVCache, pos, append=True, pad=None):
     _load().or_decode_attn_g4(_p(qkv), qkv.shape[1], kc, vc, km, vm, cache.B,
                               cache.H, cache.d, cache.cap, int(pos),
                               1 if append else 0, None if pad is None else _p(pad), _p(out))
+    return out
+
+
+class KVCache16:
+    """One layer's uncompressed K and V cache: fp16 [B][H][cap][d] each."""
+
+    def __init__(self, B, H, d, cap):
+        self.B, self.H, self.d, self.cap = B, H, d, cap
+        self.k = np.zeros((B, H, cap, d), np.float16)
+        self.v = np.zeros((B, H, cap, d), np.float16)
+
+    def view(self, b0, b1):
+        """Sequences [b0, b1) as a cache sharing this one's storage."""
+        v = KVCache16.__new__(KVCache16)
+        v.B, v.H, v.d, v.cap = b1 - b0, self.H, self.d, self.cap
+        v.k, v.v = self.k[b0:b1], self.v[b0:b1]
+        return v
+
+
+def kv_store_prefill_f16(qkv, B, s, cache: KVCache16):
+    qkv = _c(qkv, np.float16)
+    assert qkv.shape == (B * s, 3 * cache.H * cache.d) and s <= cache.cap
+    _load().or_kv_store_prefill_f16(_p(qkv), B, s, _p(cache.k), _p(cache.v), cache.H, cache.d,
+                                    cache.cap)
+
+
+def decode_attn_f16(qkv, cache: KVCache16, pos, append=True, pad=None):
+    """Decode attention over the fp16 cache (rows read as stored); qkv
+    [B][>=3*h1] fp16, pad None or [B]."""
+    qkv = _c(qkv, np.float16)
+    B = qkv.shape[0]
+    assert B == cache.B and 0 <= pos < cache.cap
+    out = np.empty((B, cache.H * cache.d), np.float16)
+    pad = _pad(pad, B)
+    _load().or_decode_attn_f16(_p(qkv), qkv.shape[1], _p(cache.k), _p(cache.v), cache.B, cache.H,
+                               cache.d, cache.cap, int(pos), 1 if append else 0,
+                               None if pad is None else _p(pad), _p(out))
     return out
 
 

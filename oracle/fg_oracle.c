@@ -493,6 +493,73 @@ void or_decode_attn_g4(const uint16_t* qkv, int64_t qkv_ld, uint8_t* k_codes,
     }
 }
 
+/* Uncompressed (fp16) KV cache: k, v [B][H][cap][d] fp16, the rows stored as
+ * the QKV projection produced them.  This is the setting the pages compare
+ * the 4-bit cache against ("FlexGen 完全拆解", results for input length 512:
+ * FlexGen with and without 4-bit compression). */
+
+/* Prefill store into the fp16 cache: token t of sequence b (row b*s + t of
+ * qkv, [B*s][3*h1]) goes to slot t. */
+void or_kv_store_prefill_f16(const uint16_t* qkv, int32_t B, int32_t s, uint16_t* k,
+                             uint16_t* v, int32_t H, int32_t d, int32_t cap)
+{
+    int64_t h1 = (int64_t)H * d, ld = 3 * h1;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t t = 0; t < s; ++t)
+            for (int64_t h = 0; h < H; ++h) {
+                int64_t row = ((b * H + h) * cap + t) * d;
+                memcpy(k + row, qkv + (b * s + t) * ld + h1 + h * d, sizeof(uint16_t) * (size_t)d);
+                memcpy(v + row, qkv + (b * s + t) * ld + 2 * h1 + h * d, sizeof(uint16_t) * (size_t)d);
+            }
+}
+
+/* Decode attention over the fp16 cache: optionally store the new k, v rows
+ * (qkv row b) into slot pos, then for each (b, h) attend slots pad[b]..pos:
+ * the same fp32 arithmetic as or_decode_attn_g4 with the cached rows read
+ * as stored instead of dequantised. */
+void or_decode_attn_f16(const uint16_t* qkv, int64_t qkv_ld, uint16_t* k, uint16_t* v,
+                        int32_t B, int32_t H, int32_t d, int32_t cap, int32_t pos,
+                        int32_t do_append, const int32_t* pad, uint16_t* out)
+{
+    int64_t h1 = (int64_t)H * d, L = (int64_t)pos + 1;
+    float scale = 1.0f / sqrtf((float)d);
+    if (do_append)
+        for (int64_t b = 0; b < B; ++b)
+            for (int64_t h = 0; h < H; ++h) {
+                int64_t row = ((b * H + h) * cap + pos) * d;
+                memcpy(k + row, qkv + b * qkv_ld + h1 + h * d, sizeof(uint16_t) * (size_t)d);
+                memcpy(v + row, qkv + b * qkv_ld + 2 * h1 + h * d, sizeof(uint16_t) * (size_t)d);
+            }
+#pragma omp parallel
+    {
+        float* q = (float*)malloc(sizeof(float) * (size_t)d);
+        float* kr = (float*)malloc(sizeof(float) * (size_t)d);
+        float* sc = (float*)malloc(sizeof(float) * (size_t)L);
+        float* p = (float*)malloc(sizeof(float) * (size_t)L);
+        float* vr = (float*)malloc(sizeof(float) * (size_t)L * (size_t)d);
+#pragma omp for collapse(2) schedule(static)
+        for (int64_t b = 0; b < B; ++b)
+            for (int64_t h = 0; h < H; ++h) {
+                const int64_t p0 = pad ? pad[b] : 0;
+                const int64_t base = (b * H + h) * cap;
+                or_h2f_array(qkv + b * qkv_ld + h * d, q, d);
+                for (int64_t j = p0; j < L; ++j) {
+                    or_h2f_array(k + (base + j) * d, kr, d);
+                    float dot = 0.0f;
+                    for (int64_t i = 0; i < d; ++i) dot += q[i] * kr[i];
+                    sc[j - p0] = dot * scale;
+                    or_h2f_array(v + (base + j) * d, vr + (j - p0) * d, d);
+                }
+                softmax_weighted(sc, vr, L - p0, d, p, out + b * h1 + h * d);
+            }
+        free(q);
+        free(kr);
+        free(sc);
+        free(p);
+        free(vr);
+    }
+}
+
 /* Number of rows kept by top-K sparse attention over n attended rows: the
  * keep_pct percent with the highest scores, rounded up (at least one row). */
 int32_t or_topk_count(int64_t n, int32_t keep_pct)

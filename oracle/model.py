@@ -38,7 +38,8 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from . import (GROUP, KVCache, argmax, decode_attn_g4, embed, kv_store_prefill,
+from . import (GROUP, KVCache, KVCache16, argmax, decode_attn_f16, decode_attn_g4, embed,
+               kv_store_prefill, kv_store_prefill_f16,
                layernorm, linear_f16_f32out, linear_g4, prefill_attn,
                quantize_g4)
 
@@ -117,12 +118,13 @@ def layer_step(L: OracleLayer, x, cache: KVCache, phase: int, B: int, T: int,
     """
     a = layernorm(x, L.ln1_g, L.ln1_b, L.eps)
     qkv = linear_g4(a, *L.qkv, bias=L.b_qkv)
+    f16 = isinstance(cache, KVCache16)   # uncompressed cache (the A/B setting)
     if phase == PREFILL:
         attn = prefill_attn(qkv, B, T, L.H, L.d, pad=pad)
-        kv_store_prefill(qkv, B, T, cache)
+        (kv_store_prefill_f16 if f16 else kv_store_prefill)(qkv, B, T, cache)
     else:
         assert T == 1
-        attn = decode_attn_g4(qkv, cache, pos, append=True, pad=pad)
+        attn = (decode_attn_f16 if f16 else decode_attn_g4)(qkv, cache, pos, append=True, pad=pad)
     h = linear_g4(attn, *L.out, bias=L.b_out, residual=x)
     u = linear_g4(layernorm(h, L.ln2_g, L.ln2_b, L.eps), *L.fc1, bias=L.b_fc1, act=1)
     y = linear_g4(u, *L.fc2, bias=L.b_fc2, residual=h)
@@ -149,9 +151,11 @@ class OracleModel:
     def h1(self):
         return self.e_tok.shape[1]
 
-    def new_caches(self, B, cap):
+    def new_caches(self, B, cap, kv="g4"):
+        """kv "g4": the 4-bit cache; "f16": the uncompressed one."""
         L0 = self.layers[0]
-        return [KVCache(B, L0.H, L0.d, cap) for _ in self.layers]
+        cls = KVCache16 if kv == "f16" else KVCache
+        return [cls(B, L0.H, L0.d, cap) for _ in self.layers]
 
     def head(self, x):
         """Final LayerNorm then logits against the tied token embedding (fp32)."""
