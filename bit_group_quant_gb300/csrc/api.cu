@@ -73,6 +73,45 @@ fg_kv4 sub_cache(const fg_kv4* c, int32_t b0, int32_t nb) {
     return s;
 }
 
+fg_status check_kv16(const fg_kv16* c, const char* what) {
+    FG_REQUIRE(c != nullptr, FG_ERR_NULL, "%s: null cache", what);
+    FG_REQUIRE(c->k && c->v, FG_ERR_NULL, "%s: null cache buffer", what);
+    FG_REQUIRE(c->d == 64 || c->d == 128, FG_ERR_UNSUPPORTED, "%s: head dim %d not in {64,128}",
+               what, c->d);
+    FG_REQUIRE(c->B >= 0 && c->H > 0 && c->cap > 0, FG_ERR_SHAPE, "%s: bad B/H/cap", what);
+    FG_REQUIRE(fg::aligned16(c->k) && fg::aligned16(c->v), FG_ERR_ALIGN,
+               "%s: cache buffers must be 16-byte aligned", what);
+    return FG_OK;
+}
+
+fg_kv16 sub_cache(const fg_kv16* c, int32_t b0, int32_t nb) {
+    fg_kv16 s = *c;
+    const int64_t el = static_cast<int64_t>(b0) * c->H * c->cap * c->d;
+    s.k = c->k + el;
+    s.v = c->v + el;
+    s.B = nb;
+    return s;
+}
+
+// The cache-specific steps of a layer: the prefill's store of the prompt's
+// K/V rows and the decode step's attention (append fused).
+fg_status kv_prefill_store(const __half* qkv, int64_t ld, int32_t nb, int32_t T, int32_t Hh,
+                           int32_t d, const fg_kv4* c, cudaStream_t st) {
+    return fg::launch_kv_store(qkv, ld, nb, T, Hh, d, c, 0, st);
+}
+fg_status kv_prefill_store(const __half* qkv, int64_t ld, int32_t, int32_t T, int32_t, int32_t,
+                           const fg_kv16* c, cudaStream_t st) {
+    return fg::launch_kv_store_f16(qkv, ld, T, c, 0, st);
+}
+fg_status kv_decode_attn(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
+                         const int32_t* pad, int32_t topk_pct, __half* out, cudaStream_t st) {
+    return fg::launch_decode_attn(qkv, ld, c, pos, pad, 1, topk_pct, nullptr, out, st);
+}
+fg_status kv_decode_attn(const __half* qkv, int64_t ld, const fg_kv16* c, int32_t pos,
+                         const int32_t* pad, int32_t, __half* out, cudaStream_t st) {
+    return fg::launch_decode_attn_f16(qkv, ld, c, pos, pad, 1, out, st);
+}
+
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct LayerWs {
@@ -246,6 +285,90 @@ TraceScope::~TraceScope() {
 }
 
 }  // namespace fg
+
+// One decoder layer over either cache kind (Cache = fg_kv4 or fg_kv16); the
+// cache is validated by the caller.
+template <class Cache>
+fg_status layer_step_impl(const fg_layer* w, const Cache* cache, const fg_f16* x_in, fg_f16* x_out,
+                          int32_t phase, int32_t T, int32_t pos, const int32_t* pad, fg_policy p,
+                          void* workspace, size_t ws_bytes, fg_stream stream) {
+    fg_status s = check_layer(w);
+    if (s != FG_OK) return s;
+    FG_REQUIRE(x_in && x_out, FG_ERR_NULL, "layer_step: null x_in or x_out");
+    FG_REQUIRE(x_in != x_out, FG_ERR_SHAPE, "layer_step: x_in and x_out may not alias");
+    FG_REQUIRE((reinterpret_cast<uintptr_t>(pad) & 3u) == 0, FG_ERR_ALIGN,
+               "layer_step: pad must be 4-byte aligned");
+    FG_REQUIRE(fg::aligned16(x_in) && fg::aligned16(x_out), FG_ERR_ALIGN,
+               "layer_step: x_in and x_out must be 16-byte aligned");
+    FG_REQUIRE(p.gbs > 0 && p.k > 0 && p.order >= 0 && p.order <= 2, FG_ERR_SHAPE,
+               "layer_step: bad policy");
+    FG_REQUIRE(p.topk_pct >= 0 && p.topk_pct <= 100, FG_ERR_SHAPE,
+               "layer_step: topk_pct %d outside [0, 100]", p.topk_pct);
+    const int32_t bls = p.gbs * p.k;
+    FG_REQUIRE(cache->B == bls, FG_ERR_SHAPE, "layer_step: cache holds %d sequences, bls = %d",
+               cache->B, bls);
+    const int d = w->h1 / w->H;
+    FG_REQUIRE(cache->H == w->H && cache->d == d, FG_ERR_SHAPE, "layer_step: cache H/d mismatch");
+    FG_REQUIRE(phase == FG_PHASE_PREFILL || phase == FG_PHASE_DECODE, FG_ERR_SHAPE,
+               "layer_step: bad phase");
+    if (phase == FG_PHASE_PREFILL) {
+        FG_REQUIRE(T >= 1 && T <= cache->cap, FG_ERR_SHAPE, "layer_step: prefill T %d outside [1, cap]", T);
+    } else {
+        FG_REQUIRE(T == 1, FG_ERR_SHAPE, "layer_step: decode needs T == 1");
+        FG_REQUIRE(pos >= 0 && pos < cache->cap, FG_ERR_SHAPE, "layer_step: pos %d outside [0, %d)",
+                   pos, cache->cap);
+    }
+    const int64_t rows = static_cast<int64_t>(bls) * T;
+    const int64_t per = p.order == FG_ORDER_BLOCK ? rows : static_cast<int64_t>(p.gbs) * T;
+    const LayerWs need = layer_ws_layout(w, rows, per, nullptr);
+    FG_REQUIRE(workspace != nullptr && ws_bytes >= need.total, FG_ERR_WORKSPACE,
+               "layer_step: workspace %zu < %zu bytes", ws_bytes, need.total);
+    FG_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, FG_ERR_ALIGN,
+               "layer_step: workspace must be 256-byte aligned");
+    const LayerWs L = layer_ws_layout(w, rows, per, static_cast<char*>(workspace));
+    const cudaStream_t st = S(stream);
+    const int64_t h1 = w->h1;
+
+    const int nbatch = p.order == FG_ORDER_BLOCK ? 1 : p.k;
+    const int32_t nb = p.order == FG_ORDER_BLOCK ? bls : p.gbs;
+    for (int it = 0; it < nbatch; ++it) {
+        const int bi = p.order == FG_ORDER_BATCHES_REV ? nbatch - 1 - it : it;
+        const int32_t b0 = bi * nb;
+        const int64_t r0 = static_cast<int64_t>(b0) * T, nr = static_cast<int64_t>(nb) * T;
+        const Cache c = sub_cache(cache, b0, nb);
+        const int32_t* pb = pad ? pad + b0 : nullptr;
+        const __half* xin = H(x_in) + r0 * h1;
+        __half* xout = Hm(x_out) + r0 * h1;
+        __half* a = L.a + r0 * h1;
+        __half* qkv = L.qkv + r0 * 3 * h1;
+        __half* attn = L.attn + r0 * h1;
+        __half* hh = L.h + r0 * h1;
+        __half* u = L.u + r0 * w->h2;
+#define FG_RUN(expr)                     \
+    do {                                 \
+        fg_status _s = (expr);           \
+        if (_s != FG_OK) return _s;      \
+    } while (0)
+        FG_RUN(fg::launch_layernorm(xin, nr, h1, h1, H(w->ln1_g), H(w->ln1_b), w->ln_eps, a, st));
+        FG_RUN(fg::launch_gemm_g4(a, nr, &w->qkv, H(w->b_qkv), nullptr, FG_ACT_NONE, qkv, L.gemm,
+                                  L.gemm_bytes, st, rows));
+        if (phase == FG_PHASE_PREFILL) {
+            FG_RUN(fg::launch_prefill_attn(qkv, nb, T, w->H, d, pb, attn, st));
+            FG_RUN(kv_prefill_store(qkv, 3 * h1, nb, T, w->H, d, &c, st));
+        } else {
+            FG_RUN(kv_decode_attn(qkv, 3 * h1, &c, pos, pb, p.topk_pct, attn, st));
+        }
+        FG_RUN(fg::launch_gemm_g4(attn, nr, &w->out, H(w->b_out), xin, FG_ACT_NONE, hh, L.gemm,
+                                  L.gemm_bytes, st, rows));
+        FG_RUN(fg::launch_layernorm(hh, nr, h1, h1, H(w->ln2_g), H(w->ln2_b), w->ln_eps, a, st));
+        FG_RUN(fg::launch_gemm_g4(a, nr, &w->fc1, H(w->b_fc1), nullptr, FG_ACT_RELU, u, L.gemm,
+                                  L.gemm_bytes, st, rows));
+        FG_RUN(fg::launch_gemm_g4(u, nr, &w->fc2, H(w->b_fc2), hh, FG_ACT_NONE, xout, L.gemm,
+                                  L.gemm_bytes, st, rows));
+#undef FG_RUN
+    }
+    return FG_OK;
+}
 
 extern "C" {
 
@@ -513,83 +636,55 @@ size_t fg_layer_workspace_bytes(const fg_layer* w, int32_t phase, int32_t bls, i
 fg_status fg_layer_step(const fg_layer* w, const fg_kv4* cache, const fg_f16* x_in, fg_f16* x_out,
                         int32_t phase, int32_t T, int32_t pos, const int32_t* pad, fg_policy p,
                         void* workspace, size_t ws_bytes, fg_stream stream) {
-    fg_status s = check_layer(w);
+    fg_status s = check_kv(cache, "layer_step");
     if (s != FG_OK) return s;
-    if ((s = check_kv(cache, "layer_step")) != FG_OK) return s;
-    FG_REQUIRE(x_in && x_out, FG_ERR_NULL, "layer_step: null x_in or x_out");
-    FG_REQUIRE(x_in != x_out, FG_ERR_SHAPE, "layer_step: x_in and x_out may not alias");
-    FG_REQUIRE((reinterpret_cast<uintptr_t>(pad) & 3u) == 0, FG_ERR_ALIGN,
-               "layer_step: pad must be 4-byte aligned");
-    FG_REQUIRE(fg::aligned16(x_in) && fg::aligned16(x_out), FG_ERR_ALIGN,
-               "layer_step: x_in and x_out must be 16-byte aligned");
-    FG_REQUIRE(p.gbs > 0 && p.k > 0 && p.order >= 0 && p.order <= 2, FG_ERR_SHAPE,
-               "layer_step: bad policy");
-    FG_REQUIRE(p.topk_pct >= 0 && p.topk_pct <= 100, FG_ERR_SHAPE,
-               "layer_step: topk_pct %d outside [0, 100]", p.topk_pct);
-    const int32_t bls = p.gbs * p.k;
-    FG_REQUIRE(cache->B == bls, FG_ERR_SHAPE, "layer_step: cache holds %d sequences, bls = %d",
-               cache->B, bls);
-    const int d = w->h1 / w->H;
-    FG_REQUIRE(cache->H == w->H && cache->d == d, FG_ERR_SHAPE, "layer_step: cache H/d mismatch");
-    FG_REQUIRE(phase == FG_PHASE_PREFILL || phase == FG_PHASE_DECODE, FG_ERR_SHAPE,
-               "layer_step: bad phase");
-    if (phase == FG_PHASE_PREFILL) {
-        FG_REQUIRE(T >= 1 && T <= cache->cap, FG_ERR_SHAPE, "layer_step: prefill T %d outside [1, cap]", T);
-    } else {
-        FG_REQUIRE(T == 1, FG_ERR_SHAPE, "layer_step: decode needs T == 1");
-        FG_REQUIRE(pos >= 0 && pos < cache->cap, FG_ERR_SHAPE, "layer_step: pos %d outside [0, %d)",
-                   pos, cache->cap);
-    }
-    const int64_t rows = static_cast<int64_t>(bls) * T;
-    const int64_t per = p.order == FG_ORDER_BLOCK ? rows : static_cast<int64_t>(p.gbs) * T;
-    const LayerWs need = layer_ws_layout(w, rows, per, nullptr);
-    FG_REQUIRE(workspace != nullptr && ws_bytes >= need.total, FG_ERR_WORKSPACE,
-               "layer_step: workspace %zu < %zu bytes", ws_bytes, need.total);
-    FG_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, FG_ERR_ALIGN,
-               "layer_step: workspace must be 256-byte aligned");
-    const LayerWs L = layer_ws_layout(w, rows, per, static_cast<char*>(workspace));
-    const cudaStream_t st = S(stream);
-    const int64_t h1 = w->h1;
+    return layer_step_impl(w, cache, x_in, x_out, phase, T, pos, pad, p, workspace, ws_bytes, stream);
+}
 
-    const int nbatch = p.order == FG_ORDER_BLOCK ? 1 : p.k;
-    const int32_t nb = p.order == FG_ORDER_BLOCK ? bls : p.gbs;
-    for (int it = 0; it < nbatch; ++it) {
-        const int bi = p.order == FG_ORDER_BATCHES_REV ? nbatch - 1 - it : it;
-        const int32_t b0 = bi * nb;
-        const int64_t r0 = static_cast<int64_t>(b0) * T, nr = static_cast<int64_t>(nb) * T;
-        const fg_kv4 c = sub_cache(cache, b0, nb);
-        const int32_t* pb = pad ? pad + b0 : nullptr;
-        const __half* xin = H(x_in) + r0 * h1;
-        __half* xout = Hm(x_out) + r0 * h1;
-        __half* a = L.a + r0 * h1;
-        __half* qkv = L.qkv + r0 * 3 * h1;
-        __half* attn = L.attn + r0 * h1;
-        __half* hh = L.h + r0 * h1;
-        __half* u = L.u + r0 * w->h2;
-#define FG_RUN(expr)                     \
-    do {                                 \
-        fg_status _s = (expr);           \
-        if (_s != FG_OK) return _s;      \
-    } while (0)
-        FG_RUN(fg::launch_layernorm(xin, nr, h1, h1, H(w->ln1_g), H(w->ln1_b), w->ln_eps, a, st));
-        FG_RUN(fg::launch_gemm_g4(a, nr, &w->qkv, H(w->b_qkv), nullptr, FG_ACT_NONE, qkv, L.gemm,
-                                  L.gemm_bytes, st, rows));
-        if (phase == FG_PHASE_PREFILL) {
-            FG_RUN(fg::launch_prefill_attn(qkv, nb, T, w->H, d, pb, attn, st));
-            FG_RUN(fg::launch_kv_store(qkv, 3 * h1, nb, T, w->H, d, &c, 0, st));
-        } else {
-            FG_RUN(fg::launch_decode_attn(qkv, 3 * h1, &c, pos, pb, 1, p.topk_pct, nullptr, attn, st));
-        }
-        FG_RUN(fg::launch_gemm_g4(attn, nr, &w->out, H(w->b_out), xin, FG_ACT_NONE, hh, L.gemm,
-                                  L.gemm_bytes, st, rows));
-        FG_RUN(fg::launch_layernorm(hh, nr, h1, h1, H(w->ln2_g), H(w->ln2_b), w->ln_eps, a, st));
-        FG_RUN(fg::launch_gemm_g4(a, nr, &w->fc1, H(w->b_fc1), nullptr, FG_ACT_RELU, u, L.gemm,
-                                  L.gemm_bytes, st, rows));
-        FG_RUN(fg::launch_gemm_g4(u, nr, &w->fc2, H(w->b_fc2), hh, FG_ACT_NONE, xout, L.gemm,
-                                  L.gemm_bytes, st, rows));
-#undef FG_RUN
-    }
-    return FG_OK;
+fg_status fg_layer_step_kv16(const fg_layer* w, const fg_kv16* cache, const fg_f16* x_in,
+                             fg_f16* x_out, int32_t phase, int32_t T, int32_t pos,
+                             const int32_t* pad, fg_policy p, void* workspace, size_t ws_bytes,
+                             fg_stream stream) {
+    fg_status s = check_kv16(cache, "layer_step_kv16");
+    if (s != FG_OK) return s;
+    FG_REQUIRE(p.topk_pct == 0, FG_ERR_UNSUPPORTED,
+               "layer_step_kv16: top-K attention (topk_pct %d) needs the 4-bit cache", p.topk_pct);
+    FG_REQUIRE(cache->cap <= 50000, FG_ERR_UNSUPPORTED, "layer_step_kv16: cap %d > 50000", cache->cap);
+    return layer_step_impl(w, cache, x_in, x_out, phase, T, pos, pad, p, workspace, ws_bytes, stream);
+}
+
+fg_status fg_kv_store_f16(const fg_f16* qkv, int64_t qkv_ld, int32_t T, const fg_kv16* cache,
+                          int32_t slot0, fg_stream stream) {
+    fg_status s = check_kv16(cache, "kv_store_f16");
+    if (s != FG_OK) return s;
+    FG_REQUIRE(qkv != nullptr, FG_ERR_NULL, "kv_store_f16: null qkv");
+    const int64_t h1 = static_cast<int64_t>(cache->H) * cache->d;
+    FG_REQUIRE(qkv_ld >= 3 * h1 && qkv_ld % 8 == 0, FG_ERR_SHAPE,
+               "kv_store_f16: qkv_ld %lld must be >= 3*h1 and a multiple of 8", (long long)qkv_ld);
+    FG_REQUIRE(T >= 0 && slot0 >= 0 && static_cast<int64_t>(slot0) + T <= cache->cap, FG_ERR_SHAPE,
+               "kv_store_f16: slots [%d, %d + %d) outside [0, %d)", slot0, slot0, T, cache->cap);
+    FG_REQUIRE(fg::aligned16(qkv), FG_ERR_ALIGN, "kv_store_f16: qkv must be 16-byte aligned");
+    return fg::launch_kv_store_f16(H(qkv), qkv_ld, T, cache, slot0, S(stream));
+}
+
+fg_status fg_decode_attn_f16(const fg_f16* qkv, int64_t qkv_ld, const fg_kv16* cache, int32_t pos,
+                             const int32_t* pad, int32_t fuse_append, fg_f16* out,
+                             fg_stream stream) {
+    fg_status s = check_kv16(cache, "decode_attn_f16");
+    if (s != FG_OK) return s;
+    FG_REQUIRE(qkv && out, FG_ERR_NULL, "decode_attn_f16: null qkv or out");
+    const int64_t h1 = static_cast<int64_t>(cache->H) * cache->d;
+    FG_REQUIRE(qkv_ld >= 3 * h1 && qkv_ld % 8 == 0, FG_ERR_SHAPE,
+               "decode_attn_f16: qkv_ld %lld must be >= 3*h1 and a multiple of 8", (long long)qkv_ld);
+    FG_REQUIRE(pos >= 0 && pos < cache->cap, FG_ERR_SHAPE,
+               "decode_attn_f16: pos %d outside [0, %d)", pos, cache->cap);
+    FG_REQUIRE(cache->cap <= 50000, FG_ERR_UNSUPPORTED, "decode_attn_f16: cap %d > 50000", cache->cap);
+    FG_REQUIRE(fg::aligned16(qkv) && fg::aligned16(out), FG_ERR_ALIGN,
+               "decode_attn_f16: qkv and out must be 16-byte aligned");
+    FG_REQUIRE((reinterpret_cast<uintptr_t>(pad) & 3u) == 0, FG_ERR_ALIGN,
+               "decode_attn_f16: pad must be 4-byte aligned");
+    return fg::launch_decode_attn_f16(H(qkv), qkv_ld, cache, pos, pad, fuse_append, Hm(out),
+                                      S(stream));
 }
 
 }  // extern "C"

@@ -67,6 +67,13 @@ fg_status launch_decode_attn(const __half* qkv, int64_t ld, const fg_kv4* c, int
                              const int32_t* pad, int32_t fuse_append, int32_t keep_pct,
                              int32_t* sel_out, __half* out, cudaStream_t st);
 int32_t decode_topk_kmax(int32_t pos, int32_t keep_pct);
+// The uncompressed (fp16) cache: store of T rows per sequence at slot0, and
+// decode attention with the append fused.
+fg_status launch_kv_store_f16(const __half* qkv, int64_t ld, int32_t T, const fg_kv16* c,
+                              int32_t slot0, cudaStream_t st);
+fg_status launch_decode_attn_f16(const __half* qkv, int64_t ld, const fg_kv16* c, int32_t pos,
+                                 const int32_t* pad, int32_t fuse_append, __half* out,
+                                 cudaStream_t st);
 fg_status launch_prefill_attn(const __half* qkv, int32_t B, int32_t s, int32_t H, int32_t d,
                               const int32_t* pad, __half* out, cudaStream_t st);
 

@@ -29,7 +29,8 @@ EXPORTS = (
     "fg_gemm_f16_f32out", "fg_layernorm", "fg_embed", "fg_kv_append_g4",
     "fg_decode_attn_g4", "fg_prefill_attn", "fg_layer_workspace_bytes", "fg_layer_step",
     "fg_debug_set", "fg_trace_begin", "fg_trace_end", "fg_dequant_gemm_g4_noalloc",
-    "fg_argmax", "fg_decode_attn_topk_g4", "fg_topk_count",
+    "fg_argmax", "fg_decode_attn_topk_g4", "fg_topk_count", "fg_kv_store_f16",
+    "fg_decode_attn_f16", "fg_layer_step_kv16",
 )
 
 
@@ -49,6 +50,11 @@ class c_kv4(ctypes.Structure):
                 ("k_meta", ctypes.c_void_p), ("v_meta", ctypes.c_void_p),
                 ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("d", ctypes.c_int32),
                 ("cap", ctypes.c_int32)]
+
+
+class c_kv16(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("B", ctypes.c_int32),
+                ("H", ctypes.c_int32), ("d", ctypes.c_int32), ("cap", ctypes.c_int32)]
 
 
 class c_policy(ctypes.Structure):
@@ -111,6 +117,10 @@ def load(path: str = LIB_PATH):
             "fg_decode_attn_topk_g4": ([P, I64, ctypes.POINTER(c_kv4), I32, P, I32, I32, P, P, P],
                                        st),
             "fg_topk_count": ([I32, I32], I32),
+            "fg_kv_store_f16": ([P, I64, I32, ctypes.POINTER(c_kv16), I32, P], st),
+            "fg_decode_attn_f16": ([P, I64, ctypes.POINTER(c_kv16), I32, P, I32, P, P], st),
+            "fg_layer_step_kv16": ([ctypes.POINTER(c_layer), ctypes.POINTER(c_kv16), P, P, I32,
+                                    I32, I32, P, c_policy, P, SZ, P], st),
             "fg_prefill_attn": ([P, I32, I32, I32, I32, P, ctypes.POINTER(c_kv4), P, P], st),
             "fg_layer_workspace_bytes": ([ctypes.POINTER(c_layer), I32, I32, I32, c_policy], SZ),
             "fg_layer_step": ([ctypes.POINTER(c_layer), ctypes.POINTER(c_kv4), P, P, I32, I32,
@@ -209,6 +219,30 @@ class KV4:
     @property
     def nbytes(self):
         return 2 * (self.k_codes.numel() + self.k_meta.numel() * 4)
+
+
+@dataclass
+class KV16:
+    """One layer's uncompressed K/V cache: k, v fp16 [B][H][cap][d]."""
+    k: torch.Tensor
+    v: torch.Tensor
+    B: int
+    H: int
+    d: int
+    cap: int
+
+    @staticmethod
+    def empty(B, H, d, cap, device="cuda", zero=True):
+        mk = torch.zeros if zero else torch.empty
+        return KV16(mk((B, H, cap, d), dtype=torch.float16, device=device),
+                    mk((B, H, cap, d), dtype=torch.float16, device=device), B, H, d, cap)
+
+    def c(self):
+        return c_kv16(_ptr(self.k), _ptr(self.v), self.B, self.H, self.d, self.cap)
+
+    @property
+    def nbytes(self):
+        return 2 * self.k.numel() * 2
 
 
 # ---------------------------------------------------------------------------
@@ -396,10 +430,28 @@ def fg_layer_workspace_bytes(layer_c: c_layer, phase, bls, T, policy: c_policy) 
                                                int(T), policy))
 
 
-def fg_layer_step(layer_c: c_layer, cache: KV4, x_in, x_out, phase, T, pos,
-                  policy: c_policy, workspace, stream=None, pad=None):
+def fg_kv_store_f16(qkv, T, cache: KV16, slot0=0, stream=None):
+    _ok(load().fg_kv_store_f16(_ptr(qkv), qkv.shape[1], int(T), ctypes.byref(cache.c()),
+                               int(slot0), _stream(stream)))
+
+
+def fg_decode_attn_f16(qkv, cache: KV16, pos, fuse_append=True, out=None, stream=None, pad=None):
+    if out is None:
+        out = torch.empty((qkv.shape[0], cache.H * cache.d), dtype=torch.float16,
+                          device=qkv.device)
     c = cache.c()
-    _ok(load().fg_layer_step(ctypes.byref(layer_c), ctypes.byref(c), _ptr(x_in), _ptr(x_out),
+    _ok(load().fg_decode_attn_f16(_ptr(qkv), qkv.shape[1], ctypes.byref(c), int(pos),
+                                  _pad(pad, cache.B), 1 if fuse_append else 0, _ptr(out),
+                                  _stream(stream)))
+    return out
+
+
+def fg_layer_step(layer_c: c_layer, cache, x_in, x_out, phase, T, pos,
+                  policy: c_policy, workspace, stream=None, pad=None):
+    """cache: KV4 (4-bit) or KV16 (fp16): fg_layer_step or fg_layer_step_kv16."""
+    c = cache.c()
+    fn = load().fg_layer_step_kv16 if isinstance(cache, KV16) else load().fg_layer_step
+    _ok(fn(ctypes.byref(layer_c), ctypes.byref(c), _ptr(x_in), _ptr(x_out),
                              int(phase), int(T), int(pos), _pad(pad, cache.B), policy,
                              _ptr(workspace), workspace.numel() * workspace.element_size(),
                              _stream(stream)))

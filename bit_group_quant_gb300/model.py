@@ -87,7 +87,7 @@ class LayerStack:
 
     topk_pct = 0
 
-    def __init__(self, layers, gbs: int, k: int, cap: int, device="cuda"):
+    def __init__(self, layers, gbs: int, k: int, cap: int, device="cuda", kv="g4"):
         self.layers = layers
         self.c_layers = [L.c() for L in layers]
         self.gbs, self.k, self.cap = gbs, k, cap
@@ -95,12 +95,18 @@ class LayerStack:
         self.h1, self.H, self.h2 = L0.h1, L0.H, L0.h2
         self.d = self.h1 // self.H
         self.device = device
-        self.caches = [fg.KV4.empty(self.bls, self.H, self.d, cap, device) for _ in layers]
+        self.kv = kv
+        self.caches = [self.new_cache(cap, device) for _ in layers]
         self._ws = {}
 
     @property
     def bls(self):
         return self.gbs * self.k
+
+    def new_cache(self, cap, device):
+        """kv "g4": the 4-bit cache; "f16": the uncompressed one (the A/B)."""
+        cls = fg.KV16 if self.kv == "f16" else fg.KV4
+        return cls.empty(self.bls, self.H, self.d, cap, device)
 
     def policy(self, order_code: int) -> fg.c_policy:
         return fg.c_policy(self.gbs, self.k, order_code, self.topk_pct)
@@ -213,13 +219,15 @@ def random_layers(wl, gen, device="cuda", affine=False, n_layers=None):
     return layers
 
 
-def random_model(wl, seed=0, device="cuda", n_layers=None, cap=None, host_weights=False):
+def random_model(wl, seed=0, device="cuda", n_layers=None, cap=None, host_weights=False,
+                 kv="g4"):
     """host_weights: keep the 4-bit weights in pinned host memory and stream
-    them one layer ahead (HostLayerStack)."""
+    them one layer ahead (HostLayerStack).  kv: "g4" (4-bit KV cache) or
+    "f16" (uncompressed)."""
     gen = synth.generator(seed, device)
     layers = random_layers(wl, gen, device, n_layers=n_layers)
     cls = HostLayerStack if host_weights else LayerStack
-    stack = cls(layers, wl.gbs, wl.k, cap or wl.cap, device)
+    stack = cls(layers, wl.gbs, wl.k, cap or wl.cap, device, kv=kv)
     e_tok, e_pos = synth.embeddings(wl.vocab, wl.cap, wl.h1, gen, device)
     ones = torch.ones(wl.h1, dtype=torch.float16, device=device)
     zeros = torch.zeros(wl.h1, dtype=torch.float16, device=device)
@@ -270,7 +278,7 @@ class HostLayerStack(LayerStack):
             out[nm] = fg.Q4(codes, meta, rows, cols)
         return out
 
-    def __init__(self, layers, gbs: int, k: int, cap: int, device="cuda"):
+    def __init__(self, layers, gbs: int, k: int, cap: int, device="cuda", kv="g4"):
         L0 = layers[0]
         self.layout, self.bytes_per_layer = self._layout(L0)
         # host copies of the quantised projections, one pinned buffer per
@@ -292,7 +300,8 @@ class HostLayerStack(LayerStack):
         self.h1, self.H, self.h2 = L0.h1, L0.H, L0.h2
         self.d = self.h1 // self.H
         self.device = device
-        self.caches = [fg.KV4.empty(self.bls, self.H, self.d, cap, device) for _ in layers]
+        self.kv = kv
+        self.caches = [self.new_cache(cap, device) for _ in layers]
         self._ws = {}
         self.copy_stream = torch.cuda.Stream(device)
         self.freed = [torch.cuda.Event(), torch.cuda.Event()]

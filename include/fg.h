@@ -94,6 +94,16 @@ typedef struct fg_kv4 {
     int32_t B, H, d, cap;
 } fg_kv4;
 
+/* One layer's uncompressed KV cache (the setting the pages compare the 4-bit
+ * cache against, "FlexGen 完全拆解", results for input length 512): k and v
+ * fp16 [B][H][cap][d], each row as the QKV projection produced it.  d in
+ * {64, 128}; k and v 16-byte aligned. */
+typedef struct fg_kv16 {
+    fg_f16* k;
+    fg_f16* v;
+    int32_t B, H, d, cap;
+} fg_kv16;
+
 /* Block schedule: bls = gbs * k sequences per block.
  * order FG_ORDER_BLOCK: each projection is ONE launch over all bls rows, so
  *   each weight tile is fetched from HBM and dequantised once per block.
@@ -289,6 +299,28 @@ fg_status fg_decode_attn_topk_g4(const fg_f16* qkv, int64_t qkv_ld,
                                  int32_t fuse_append, fg_f16* out,
                                  int32_t* sel_out, fg_stream stream);
 
+/* Store rows of k and v into the fp16 cache: token t (0 <= t < T) of
+ * sequence b, row b*T + t of qkv ([B*T][qkv_ld] fp16 holding q | k | v of
+ * width h1 = H*d each), goes to slot slot0 + t of sequence b, copied as is.
+ * qkv_ld >= 3*h1, qkv_ld % 8 == 0; qkv 16-byte aligned; 0 <= slot0 and
+ * slot0 + T <= cap.  The prefill stores T = s rows at slot 0; a decode step
+ * that does not fuse its append stores T = 1 row at slot pos. */
+fg_status fg_kv_store_f16(const fg_f16* qkv, int64_t qkv_ld, int32_t T,
+                          const fg_kv16* cache, int32_t slot0, fg_stream stream);
+
+/* Decode attention over the fp16 cache: for each sequence b and head h,
+ * out = sum_j softmax_j(q . k_j / sqrt(d)) v_j over slots j = pad[b]..pos
+ * (pad NULL: 0..pos), the rows read as stored.  If fuse_append != 0 the new
+ * k, v rows (qkv row b) are first stored into slot pos, as fg_kv_store_f16
+ * with T = 1 does, in the same launch.  qkv as for fg_kv_store_f16 with
+ * B = cache->B rows; pad: NULL or [B] (4-byte aligned); out: [B][h1] fp16,
+ * 16-byte aligned.  0 <= pos < cap <= 50000.  Device waits are bounded and
+ * report FG_ERR_TIMEOUT through fg_check. */
+fg_status fg_decode_attn_f16(const fg_f16* qkv, int64_t qkv_ld,
+                             const fg_kv16* cache, int32_t pos,
+                             const int32_t* pad, int32_t fuse_append,
+                             fg_f16* out, fg_stream stream);
+
 /* Rows kept by top-K attention out of n: ceil(n * keep_pct / 100) (at least
  * one for n >= 1).  Returns -1 for n < 0 or keep_pct outside [1, 100]. */
 int32_t fg_topk_count(int32_t n, int32_t keep_pct);
@@ -324,6 +356,17 @@ fg_status fg_layer_step(const fg_layer* w, const fg_kv4* cache,
                         int32_t T, int32_t pos, const int32_t* pad,
                         fg_policy p, void* workspace, size_t ws_bytes,
                         fg_stream stream);
+
+/* fg_layer_step over the uncompressed fp16 cache: the same layer, schedule,
+ * workspace and errors, with the prefill storing the K/V rows as
+ * fg_kv_store_f16 does and each decode step attending as fg_decode_attn_f16
+ * does (append fused).  p.topk_pct must be 0 (top-K attention is an option
+ * of the 4-bit cache; FG_ERR_UNSUPPORTED otherwise). */
+fg_status fg_layer_step_kv16(const fg_layer* w, const fg_kv16* cache,
+                             const fg_f16* x_in, fg_f16* x_out, int32_t phase,
+                             int32_t T, int32_t pos, const int32_t* pad,
+                             fg_policy p, void* workspace, size_t ws_bytes,
+                             fg_stream stream);
 
 /* ------------------------------------------------------------------ tracing */
 

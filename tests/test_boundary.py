@@ -76,6 +76,17 @@ def test_host_validation_rejects_without_launch(lib):
     for n, pct, want in [(513, 10, 52), (1, 10, 1), (10, 10, 1), (11, 10, 2), (7, 100, 7),
                          (0, 10, 0), (5, 0, -1), (5, 101, -1), (-1, 10, -1)]:
         assert lib.fg_topk_count(n, pct) == want
+    kv16 = fg.c_kv16(P(0x1000), P(0x2000), 2, 2, 96, 8)                      # d = 96
+    assert lib.fg_decode_attn_f16(P(0x5000), 576, ctypes.byref(kv16), 0, None, 1, P(0x6000),
+                                  None) == fg.FG_ERR_UNSUPPORTED
+    kv16 = fg.c_kv16(P(0x1000), P(0x2008), 2, 2, 64, 8)                      # v misaligned
+    assert lib.fg_kv_store_f16(P(0x5000), 384, 1, ctypes.byref(kv16), 0, None) == fg.FG_ERR_ALIGN
+    kv16 = fg.c_kv16(P(0x1000), P(0x2000), 2, 2, 64, 8)
+    assert lib.fg_decode_attn_f16(P(0x5000), 384, ctypes.byref(kv16), 8, None, 1, P(0x6000),
+                                  None) == fg.FG_ERR_SHAPE                 # pos == cap
+    assert lib.fg_kv_store_f16(P(0x5000), 384, 4, ctypes.byref(kv16), 5, None) == fg.FG_ERR_SHAPE
+    assert lib.fg_kv_store_f16(P(0x5000), 100, 1, ctypes.byref(kv16), 0, None) == fg.FG_ERR_SHAPE
+    assert lib.fg_kv_store_f16(P(0x5000), 384, 0, ctypes.byref(kv16), 0, None) == fg.FG_OK
     assert lib.fg_kv_append_g4(P(0x5000), 100, ctypes.byref(kv), 0, None) == fg.FG_ERR_SHAPE
     assert lib.fg_layernorm(P(0x1000), 4, 100, 100, P(0x2000), P(0x3000), 1e-5, P(0x4000),
                             None) == fg.FG_ERR_SHAPE
@@ -116,6 +127,13 @@ def test_layer_step_validation(lib):
         st = lib.fg_layer_step(ctypes.byref(L), ctypes.byref(kv), P(0x5000), P(0x6000), 1, 1, 3,
                                None, fg.c_policy(2, 2, 0, bad), P(0x100000), 1 << 30, None)
         assert st == fg.FG_ERR_SHAPE and b"topk_pct" in lib.fg_last_error()
+    kv16 = fg.c_kv16(P(0x1000), P(0x2000), 4, H, 64, 16)
+    st = lib.fg_layer_step_kv16(ctypes.byref(L), ctypes.byref(kv16), P(0x5000), P(0x6000), 1, 1, 3,
+                                None, fg.c_policy(2, 2, 0, 10), P(0x100000), 1 << 30, None)
+    assert st == fg.FG_ERR_UNSUPPORTED and b"4-bit" in lib.fg_last_error()
+    st = lib.fg_layer_step_kv16(ctypes.byref(L), ctypes.byref(kv16), P(0x5000), P(0x6000), 1, 1, 3,
+                                None, fg.c_policy(2, 3, 0), P(0x100000), 1 << 30, None)
+    assert st == fg.FG_ERR_SHAPE and b"bls" in lib.fg_last_error()
     L.fc1 = q(h2 + 64, h1)
     st = lib.fg_layer_step(ctypes.byref(L), ctypes.byref(kv), P(0x5000), P(0x6000), 1, 1, 3,
                            None, pol, P(0x100000), 1 << 30, None)
