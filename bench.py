@@ -239,7 +239,8 @@ def run_fg(args, ws, rank, local):
     stream = torch.cuda.current_stream()
 
     host = args.weights == "host"
-    model = random_model(wl, seed=0, device=dev, host_weights=host)
+    model = random_model(wl, seed=0, device=dev, host_weights=host, kv=args.kv)
+    model.stack.topk_pct = args.topk
     g = synth.generator(1000 + rank, dev)
     prompt = synth.token_ids((wl.bls, wl.s), wl.vocab, g, dev)
     logits_buf = [torch.empty((wl.bls, wl.vocab), dtype=torch.float32, device=dev)
@@ -378,9 +379,13 @@ def run_fg(args, ws, rank, local):
         "data": "synthetic",
         "config": {"workload": "%s-shaped: %d layers, h1 %d, %d heads, h2 %d, vocab %d; "
                                "gbs %d x k %d = bls %d, s %d, n %d (%d decode steps); "
-                               "weights and KV 4-bit g64 in HBM"
+                               "weights 4-bit g64, KV cache %s, in HBM"
                                % (wl.name, wl.layers, wl.h1, wl.H, wl.h2, wl.vocab, wl.gbs,
-                                  wl.k, wl.bls, wl.s, wl.n, D),
+                                  wl.k, wl.bls, wl.s, wl.n, D,
+                                  "fp16 (uncompressed)" if args.kv == "f16" else "4-bit g64"),
+                   "kv_cache": args.kv,
+                   "decode_attention": ("top-K sparse, %d%% of the rows' V" % args.topk
+                                        if 0 < args.topk < 100 else "dense"),
                    "order": args.order, "decoding": "greedy (argmax on the device)",
                    "parallelism": "replicas" if ws > 1 else "single",
                    "weights": ("4-bit, pinned host memory, streamed one layer ahead over "
@@ -389,7 +394,7 @@ def run_fg(args, ws, rank, local):
                          % (wbytes / 1e9, sum(c.nbytes for c in model.stack.caches) / 1e9)},
         "generation_tokens_per_s": gen_value,
         "gemm_tflops": {"prefill": tflops(gp), "decode": tflops(gd)},
-        "attn_gbs": {"decode_4bit": gbs(ad)},
+        "attn_gbs": {("decode_f16" if args.kv == "f16" else "decode_4bit"): gbs(ad)},
         "phase_ms_per_step": {"prefill": t_pre / args.steps * 1e3,
                               "decode": t_dec / args.steps * 1e3},
         "kernel_ms_per_step": {k: c["ms"] / args.steps for k, c in trace.items()},
@@ -454,13 +459,23 @@ def gemm_case(M, N, K, iters, dev, seed=0, residual=False):
     return sec, flops / sec / 1e12, bytes_ / sec / 1e9
 
 
-def attn_case(B, H, d, L, iters, dev, seed=0, topk=0):
+def attn_case(B, H, d, L, iters, dev, seed=0, topk=0, kv="g4"):
     """One decode-attention launch over a full 4-bit cache of L rows
     (fused append at slot L-1); returns (seconds, GB/s).  topk 1..99: the
     top-K sparse attention keeping that percent of the rows' V (its bytes:
-    every K row, the kept V rows)."""
+    every K row, the kept V rows).  kv "f16": the uncompressed cache."""
     from bit_group_quant_gb300 import fg
     g = synth.generator(seed, dev)
+    if kv == "f16":
+        c16 = fg.KV16.empty(B, H, d, L, dev, zero=False)
+        c16.k.copy_(synth.normal_f16((B, H, L, d), 1.0, g, dev))
+        c16.v.copy_(synth.normal_f16((B, H, L, d), 1.0, g, dev))
+        qkv = synth.normal_f16((B, 3 * H * d), 1.0, g, dev)
+        out = torch.empty((B, H * d), dtype=torch.float16, device=dev)
+        sec = _time_launches(lambda: fg.fg_decode_attn_f16(qkv, c16, L - 1, out=out), iters,
+                             torch.cuda.current_stream())
+        fg.fg_check()
+        return sec, B * H * (2.0 * L * d * 2 + 2 * d * 2 + 8.0 * d) / sec / 1e9
     cache = fg.KV4.empty(B, H, d, L, dev, zero=False)
     rows = synth.normal_f16((B * H * L, d), 1.0, g, dev)
     kq = fg.fg_quantize_g4(rows)
@@ -511,7 +526,7 @@ def decode_case(args, dev):
     if args.gbs:
         wl = dataclasses.replace(wl, gbs=args.gbs, k=args.k or 1)
     host = args.weights == "host"
-    model = random_model(wl, seed=0, device=dev, host_weights=host)
+    model = random_model(wl, seed=0, device=dev, host_weights=host, kv=args.kv)
     model.stack.topk_pct = args.topk
     D = wl.decode_steps
     toks = torch.zeros((wl.n, wl.bls), dtype=torch.int32, device=dev)
@@ -531,7 +546,8 @@ def decode_case(args, dev):
     torch.cuda.synchronize()
     fg.fg_check()
     sec = a.elapsed_time(b) / 1e3
-    return {"micro": "decode", "weights": args.weights, "topk_pct": args.topk,
+    return {"micro": "decode", "weights": args.weights, "kv": args.kv, "s": wl.s,
+            "topk_pct": args.topk,
             "bls": wl.bls, "gbs": wl.gbs, "k": wl.k,
             "decode_steps": D, "ms_per_decode_step": sec / D * 1e3,
             "host_enqueue_ms_per_decode_step": (h1 - h0) / D * 1e3,
@@ -556,8 +572,10 @@ def run_micro(args):
                 "ms": sec * 1e3, "tflops_causal": tf, "frac_tensor": tf / peaks["bf16_tflops"],
                 "peak_source": kind + " bf16_tflops"}
     if args.micro == "attn":
-        sec, gb = attn_case(args.B, args.H, args.d, args.L, args.iters, dev, topk=args.topk)
-        res = {"micro": "decode_attn_topk_g4" if 0 < args.topk < 100 else "decode_attn_g4",
+        sec, gb = attn_case(args.B, args.H, args.d, args.L, args.iters, dev, topk=args.topk,
+                            kv=args.kv)
+        res = {"micro": ("decode_attn_f16" if args.kv == "f16" else
+                         "decode_attn_topk_g4" if 0 < args.topk < 100 else "decode_attn_g4"),
                "B": args.B, "H": args.H, "d": args.d, "L": args.L,
                "ms": sec * 1e3, "gbs": gb, "frac_hbm": gb / peaks["hbm_gbs"],
                "peak_source": kind + " hbm_gbs"}
@@ -642,9 +660,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gbs", type=int, default=0, help="--micro decode: override gbs")
     ap.add_argument("--k", type=int, default=0, help="--micro decode: override k")
+    ap.add_argument("--kv", choices=["g4", "f16"], default="g4",
+                    help="KV cache: 4-bit g64 (the method) or fp16 (the uncompressed A/B)")
     ap.add_argument("--topk", type=int, default=0,
-                    help="--micro attn/decode: top-K sparse decode attention keeping this percent "
-                         "of the rows (0: dense)")
+                    help="top-K sparse decode attention keeping this percent of the rows "
+                         "(0: dense); the step, --micro attn and --micro decode")
     ap.add_argument("--micro", choices=["gemm", "attn", "prefill", "sweep175b", "decode"], default=None,
                     help="time one kernel shape (or the OPT-175B layer sweep) instead")
     ap.add_argument("--M", type=int, default=4096)

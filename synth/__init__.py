@@ -50,13 +50,15 @@ OPT125M_LAYER = Workload("opt125m-layer", 1, 768, 12, 3072, 0, 4, 1, 32, 8, 8)
 OPT1_3B = Workload("opt-1.3b", 24, 2048, 32, 8192, 50272, 16, 1, 512, 32, 31)
 OPT6_7B = Workload("opt-6.7b", 32, 4096, 32, 16384, 50272, 32, 8, 512, 32, 31)
 OPT30B = Workload("opt-30b", 48, 7168, 56, 28672, 50272, 48, 3, 512, 32, 31)
+# The same model on the pages' longer synthetic input (prompts padded to 1024).
+OPT30B_S1024 = Workload("opt-30b-s1024", 48, 7168, 56, 28672, 50272, 48, 3, 1024, 32, 31)
 # OPT-175B single-layer kernel sweep shapes.
 OPT175B_H1, OPT175B_H, OPT175B_H2 = 12288, 96, 49152
 SWEEP_GEMM_BLS = (32, 144, 256, 512)
 SWEEP_ATTN_BLS = 144
 SWEEP_ATTN_CTX = (512, 1024, 2048)
 
-WORKLOADS = {w.name: w for w in (OPT125M_LAYER, OPT1_3B, OPT6_7B, OPT30B)}
+WORKLOADS = {w.name: w for w in (OPT125M_LAYER, OPT1_3B, OPT6_7B, OPT30B, OPT30B_S1024)}
 
 
 def generator(seed: int = 0, device="cpu") -> torch.Generator:
