@@ -488,7 +488,10 @@ def attn_case(B, H, d, L, iters, dev, seed=0, topk=0, kv="g4"):
     qkv = synth.normal_f16((B, 3 * H * d), 1.0, g, dev)
     out = torch.empty((B, H * d), dtype=torch.float16, device=dev)
     if 0 < topk < 100:
-        fn = lambda: fg.fg_decode_attn_topk_g4(qkv, cache, L - 1, topk, fuse_append=True, out=out)
+        ws = torch.empty(fg.fg_decode_attn_topk_workspace_bytes(B, H, L - 1), dtype=torch.uint8,
+                         device=dev)
+        fn = lambda: fg.fg_decode_attn_topk_g4(qkv, cache, L - 1, topk, fuse_append=True, out=out,
+                                               workspace=ws)
         nv = fg.fg_topk_count(L, topk)
     else:
         fn = lambda: fg.fg_decode_attn_g4(qkv, cache, L - 1, fuse_append=True, out=out)

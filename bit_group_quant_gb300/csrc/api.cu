@@ -104,11 +104,15 @@ fg_status kv_prefill_store(const __half* qkv, int64_t ld, int32_t, int32_t T, in
     return fg::launch_kv_store_f16(qkv, ld, T, c, 0, st);
 }
 fg_status kv_decode_attn(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
-                         const int32_t* pad, int32_t topk_pct, __half* out, cudaStream_t st) {
-    return fg::launch_decode_attn(qkv, ld, c, pos, pad, 1, topk_pct, nullptr, out, st);
+                         const int32_t* pad, int32_t topk_pct, void* tk, size_t tk_bytes,
+                         __half* out, cudaStream_t st) {
+    if (topk_pct > 0 && topk_pct < 100)
+        return fg::launch_decode_attn_topk(qkv, ld, c, pos, pad, 1, topk_pct, nullptr, tk, tk_bytes,
+                                           out, st);
+    return fg::launch_decode_attn(qkv, ld, c, pos, pad, 1, out, st);
 }
 fg_status kv_decode_attn(const __half* qkv, int64_t ld, const fg_kv16* c, int32_t pos,
-                         const int32_t* pad, int32_t, __half* out, cudaStream_t st) {
+                         const int32_t* pad, int32_t, void*, size_t, __half* out, cudaStream_t st) {
     return fg::launch_decode_attn_f16(qkv, ld, c, pos, pad, 1, out, st);
 }
 
@@ -118,10 +122,20 @@ struct LayerWs {
     __half *a, *qkv, *attn, *h, *u;
     void* gemm;
     size_t gemm_bytes;
+    void* topk;          // top-K attention's scores (decode with 0 < topk_pct < 100)
+    size_t topk_bytes;
     size_t total;
 };
 
-LayerWs layer_ws_layout(const fg_layer* w, int64_t rows, int64_t rows_per_launch, char* base) {
+// Top-K scratch of one decode attention launch of nb sequences at context
+// pos + 1 (0 unless 0 < topk_pct < 100).
+size_t topk_scratch(int32_t phase, int32_t topk_pct, int64_t nb, int32_t H, int32_t pos) {
+    if (phase != FG_PHASE_DECODE || topk_pct <= 0 || topk_pct >= 100) return 0;
+    return fg::decode_topk_ws_bytes(static_cast<int32_t>(nb), H, pos);
+}
+
+LayerWs layer_ws_layout(const fg_layer* w, int64_t rows, int64_t rows_per_launch, char* base,
+                        size_t topk_bytes) {
     LayerWs L{};
     const int64_t h1 = w->h1, h2 = w->h2;
     size_t off = 0;
@@ -143,6 +157,8 @@ LayerWs layer_ws_layout(const fg_layer* w, int64_t rows, int64_t rows_per_launch
     }
     L.gemm_bytes = g;
     L.gemm = take(g);
+    L.topk_bytes = topk_bytes;
+    L.topk = take(topk_bytes);
     L.total = off;
     return L;
 }
@@ -320,12 +336,13 @@ fg_status layer_step_impl(const fg_layer* w, const Cache* cache, const fg_f16* x
     }
     const int64_t rows = static_cast<int64_t>(bls) * T;
     const int64_t per = p.order == FG_ORDER_BLOCK ? rows : static_cast<int64_t>(p.gbs) * T;
-    const LayerWs need = layer_ws_layout(w, rows, per, nullptr);
+    const size_t tk = topk_scratch(phase, p.topk_pct, per / T, w->H, pos);
+    const LayerWs need = layer_ws_layout(w, rows, per, nullptr, tk);
     FG_REQUIRE(workspace != nullptr && ws_bytes >= need.total, FG_ERR_WORKSPACE,
                "layer_step: workspace %zu < %zu bytes", ws_bytes, need.total);
     FG_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, FG_ERR_ALIGN,
                "layer_step: workspace must be 256-byte aligned");
-    const LayerWs L = layer_ws_layout(w, rows, per, static_cast<char*>(workspace));
+    const LayerWs L = layer_ws_layout(w, rows, per, static_cast<char*>(workspace), tk);
     const cudaStream_t st = S(stream);
     const int64_t h1 = w->h1;
 
@@ -356,7 +373,8 @@ fg_status layer_step_impl(const fg_layer* w, const Cache* cache, const fg_f16* x
             FG_RUN(fg::launch_prefill_attn(qkv, nb, T, w->H, d, pb, attn, st));
             FG_RUN(kv_prefill_store(qkv, 3 * h1, nb, T, w->H, d, &c, st));
         } else {
-            FG_RUN(kv_decode_attn(qkv, 3 * h1, &c, pos, pb, p.topk_pct, attn, st));
+            FG_RUN(kv_decode_attn(qkv, 3 * h1, &c, pos, pb, p.topk_pct, L.topk, L.topk_bytes, attn,
+                                  st));
         }
         FG_RUN(fg::launch_gemm_g4(attn, nr, &w->out, H(w->b_out), xin, FG_ACT_NONE, hh, L.gemm,
                                   L.gemm_bytes, st, rows));
@@ -388,7 +406,7 @@ const char* fg_status_str(fg_status s) {
 
 const char* fg_last_error(void) { return g_err; }
 
-int32_t fg_version(void) { return (3 << 16) | 0; }
+int32_t fg_version(void) { return (4 << 16) | 0; }
 
 fg_status fg_check(fg_stream stream) {
     cudaError_t e = cudaStreamSynchronize(S(stream));
@@ -570,14 +588,19 @@ fg_status fg_decode_attn_g4(const fg_f16* qkv, int64_t qkv_ld, const fg_kv4* cac
                "decode_attn_g4: qkv and out must be 16-byte aligned");
     FG_REQUIRE((reinterpret_cast<uintptr_t>(pad) & 3u) == 0, FG_ERR_ALIGN,
                "decode_attn_g4: pad must be 4-byte aligned");
-    return fg::launch_decode_attn(H(qkv), qkv_ld, cache, pos, pad, fuse_append, 0, nullptr,
-                                  Hm(out), S(stream));
+    return fg::launch_decode_attn(H(qkv), qkv_ld, cache, pos, pad, fuse_append, Hm(out),
+                                  S(stream));
+}
+
+size_t fg_decode_attn_topk_workspace_bytes(int32_t B, int32_t H, int32_t pos) {
+    if (B < 0 || H <= 0 || pos < 0) return 0;
+    return fg::decode_topk_ws_bytes(B, H, pos);
 }
 
 fg_status fg_decode_attn_topk_g4(const fg_f16* qkv, int64_t qkv_ld, const fg_kv4* cache,
                                  int32_t pos, const int32_t* pad, int32_t keep_pct,
                                  int32_t fuse_append, fg_f16* out, int32_t* sel_out,
-                                 fg_stream stream) {
+                                 void* workspace, size_t ws_bytes, fg_stream stream) {
     fg_status s = check_kv(cache, "decode_attn_topk_g4");
     if (s != FG_OK) return s;
     FG_REQUIRE(qkv && out, FG_ERR_NULL, "decode_attn_topk_g4: null qkv or out");
@@ -594,8 +617,10 @@ fg_status fg_decode_attn_topk_g4(const fg_f16* qkv, int64_t qkv_ld, const fg_kv4
     FG_REQUIRE((reinterpret_cast<uintptr_t>(pad) & 3u) == 0 &&
                    (reinterpret_cast<uintptr_t>(sel_out) & 3u) == 0,
                FG_ERR_ALIGN, "decode_attn_topk_g4: pad and sel_out must be 4-byte aligned");
-    return fg::launch_decode_attn(H(qkv), qkv_ld, cache, pos, pad, fuse_append, keep_pct, sel_out,
-                                  Hm(out), S(stream));
+    FG_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, FG_ERR_ALIGN,
+               "decode_attn_topk_g4: workspace must be 256-byte aligned");
+    return fg::launch_decode_attn_topk(H(qkv), qkv_ld, cache, pos, pad, fuse_append, keep_pct,
+                                       sel_out, workspace, ws_bytes, Hm(out), S(stream));
 }
 
 int32_t fg_topk_count(int32_t n, int32_t keep_pct) {
@@ -625,12 +650,12 @@ fg_status fg_prefill_attn(const fg_f16* qkv, int32_t B, int32_t s_len, int32_t H
 }
 
 size_t fg_layer_workspace_bytes(const fg_layer* w, int32_t phase, int32_t bls, int32_t T,
-                                fg_policy p) {
-    if (!w || bls <= 0 || T <= 0 || p.gbs <= 0 || p.k <= 0) return 0;
-    (void)phase;
+                                int32_t cap, fg_policy p) {
+    if (!w || bls <= 0 || T <= 0 || p.gbs <= 0 || p.k <= 0 || w->H <= 0) return 0;
     const int64_t rows = static_cast<int64_t>(bls) * T;
     const int64_t per = p.order == FG_ORDER_BLOCK ? rows : static_cast<int64_t>(p.gbs) * T;
-    return layer_ws_layout(w, rows, per, nullptr).total;
+    const size_t tk = cap > 0 ? topk_scratch(phase, p.topk_pct, per / T, w->H, cap - 1) : 0;
+    return layer_ws_layout(w, rows, per, nullptr, tk).total;
 }
 
 fg_status fg_layer_step(const fg_layer* w, const fg_kv4* cache, const fg_f16* x_in, fg_f16* x_out,

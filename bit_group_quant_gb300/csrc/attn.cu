@@ -101,10 +101,8 @@ __device__ __forceinline__ uint32_t score_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Shared scratch of topk_select: two 256-bin histograms, 16 ints, and up to
-// kTkCand candidate keys.
+// Candidate keys a warp ranks exactly (the scores of the cut bin).
 constexpr int kTkCand = 128;
-constexpr int kTkScratchBytes = 2 * 256 * 4 + 64 + kTkCand * 4;
 
 // Bin of a score in 256 equal bins over [mn, mx] (inv = 256 / (mx - mn)):
 // each step is monotone in s, so a higher bin holds only higher scores.
@@ -112,187 +110,307 @@ __device__ __forceinline__ uint32_t tk_bin(float s, float mn, float inv) {
     return static_cast<uint32_t>(min(max(static_cast<int>((s - mn) * inv), 0), 255));
 }
 
-// The ksel highest of the scores sc[0..L) (equal scores: lower index first)
-// as ascending indices sel[0..ksel); also returns this thread's part of the
-// softmax normaliser, sum exp(s_j - mx) over j = tid, tid + blockDim, ...
-// (the dense kernels' order), mx / mn the scores' maximum / minimum.
-// The cut is found on order-preserving keys of the scores.  Usually one
-// histogram of the scores over 256 equal bins of [mn, mx] (built in the same
-// loop as the normaliser) gives the bin holding the ksel-th highest score;
-// its scores (at most kTkCand) are ranked exactly by one warp.  Otherwise
-// (a crowded bin, or all scores equal) a radix selection finds the cut key
-// in four 8-bit digit passes over alternating histograms.  Then one pass in
-// index order keeps every key above the cut and the first `need` keys equal
-// to it: each warp owns a contiguous range of indices, counts its keys above
-// and equal to the cut, and writes its kept indices after those of the
-// warps before it.  Block-wide: every thread calls it; ends with a barrier.
-__device__ float topk_select(const float* sc, int L, int ksel, float mx, float mn, int* sel,
-                             uint8_t* scratch) {
-    constexpr int NW = kDecThreads / 32;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    uint32_t* hist = reinterpret_cast<uint32_t*>(scratch);
-    int* ws = reinterpret_cast<int*>(scratch + 2 * 256 * 4);
-    uint32_t* cand = reinterpret_cast<uint32_t*>(scratch + 2 * 256 * 4 + 64);
-    const bool all = ksel >= L;
-    const float inv = 256.0f / (mx - mn);
-    const bool binned = !all && mx > mn && inv < CUDART_INF_F;   // block-uniform
-    if (binned) {
-        for (int i = tid; i < 256; i += kDecThreads) hist[i] = 0u;
-        if (tid == 0) ws[2] = 0;
-        __syncthreads();
+// Warp-wide: the highest digit d of the 256-bin histogram hc with
+// #(keys above d) < need <= #(d and above); every lane gets d and
+// #(above d).  Lane l reads bins 255 - 8l down to 248 - 8l.
+__device__ __forceinline__ void tk_scan(const uint32_t* hc, uint32_t need, int lane,
+                                        uint32_t& digit, uint32_t& above) {
+    uint32_t c[8], cnt = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        c[i] = hc[255 - 8 * lane - i];
+        cnt += c[i];
     }
-    float lsum = 0.0f;
-    for (int j = tid; j < L; j += kDecThreads) {
-        const float sj = sc[j];
-        lsum += expf(sj - mx);
-        if (binned) atomicAdd(&hist[tk_bin(sj, mn, inv)], 1u);
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
     }
-    if (all) {
-        for (int j = tid; j < L; j += kDecThreads) sel[j] = j;
-        __syncthreads();
-        return lsum;
-    }
-    // the highest digit d of hc with #(above d) < need <= #(d and above):
-    // ws[0] = d, ws[1] = #(above d); warp 0 scans, lane l holding bins
-    // 255 - 8l .. 248 - 8l
-    auto scan = [&](const uint32_t* hc, uint32_t need) {
-        uint32_t c[8], cnt = 0u;
+    const uint32_t excl = incl - cnt;
+    const bool mine = excl < need && need <= incl;   // exactly one lane
+    uint32_t d = 0u, a = 0u, acc = excl;
+    if (mine) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            c[i] = hc[255 - 8 * lane - i];
-            cnt += c[i];
-        }
-        uint32_t incl = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        const uint32_t excl = incl - cnt;
-        if (excl < need && need <= incl) {   // exactly one lane
-            uint32_t acc = excl;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if (acc + c[i] >= need) {
-                    ws[0] = 255 - 8 * lane - i;
-                    ws[1] = static_cast<int>(acc);
-                    break;
-                }
-                acc += c[i];
+            if (acc + c[i] >= need) {
+                d = 255 - 8 * lane - i;
+                a = acc;
+                break;
             }
-        }
-    };
-    uint32_t prefix = 0u, need = static_cast<uint32_t>(ksel);
-    bool resolved = false;
-    if (binned) {
-        __syncthreads();
-        if (warp == 0) scan(hist, need);
-        __syncthreads();
-        const uint32_t bstar = static_cast<uint32_t>(ws[0]);
-        uint32_t need_b = need - static_cast<uint32_t>(ws[1]);   // kept from the cut bin
-        for (int j = tid; j < L; j += kDecThreads) {
-            const float sj = sc[j];
-            if (tk_bin(sj, mn, inv) == bstar) {
-                const int at = atomicAdd(&ws[2], 1);
-                if (at < kTkCand) cand[at] = score_key(sj);
-            }
-        }
-        __syncthreads();
-        const int nc = ws[2];
-        if (nc <= kTkCand) {
-            // the need-th highest candidate key T and how many exceed it
-            if (warp == 0) {
-                for (int i = lane; i < nc; i += 32) {
-                    const uint32_t ki = cand[i];
-                    uint32_t gt = 0u, ge = 0u;
-                    for (int m = 0; m < nc; ++m) {
-                        const uint32_t km = cand[m];
-                        gt += km > ki;
-                        ge += km >= ki;
-                    }
-                    if (gt < need_b && need_b <= ge) {   // lanes holding T agree
-                        ws[3] = static_cast<int>(ki);
-                        ws[4] = static_cast<int>(gt);
-                    }
-                }
-            }
-            __syncthreads();
-            prefix = static_cast<uint32_t>(ws[3]);
-            need = need_b - static_cast<uint32_t>(ws[4]);
-            resolved = true;
+            acc += c[i];
         }
     }
-    if (!resolved) {
-        for (int i = tid; i < 512; i += kDecThreads) hist[i] = 0u;
-        __syncthreads();
-        uint32_t pmask = 0u;
-#pragma unroll 1
-        for (int pass = 0; pass < 4; ++pass) {
-            const int shift = 24 - 8 * pass;
-            uint32_t* hc = hist + 256 * (pass & 1);
-            uint32_t* hn = hist + 256 * ((pass + 1) & 1);   // read last in pass - 1: free
-            for (int i = tid; i < 256; i += kDecThreads) hn[i] = 0u;
-            for (int j = tid; j < L; j += kDecThreads) {
-                const uint32_t k = score_key(sc[j]);
-                if ((k & pmask) == prefix) atomicAdd(&hc[(k >> shift) & 255u], 1u);
-            }
-            __syncthreads();
-            if (warp == 0) scan(hc, need);
-            __syncthreads();
-            // ws is rewritten only after the next pass's first barrier
-            prefix |= static_cast<uint32_t>(ws[0]) << shift;
-            pmask |= 0xFFu << shift;
-            need -= static_cast<uint32_t>(ws[1]);
-        }
-    }
-    // prefix: the key of the ksel-th highest score; need (>= 1) of the keys
-    // equal to it are kept, lowest index first.  Warp w owns [lo, hi).
-    const int per = (((L + NW - 1) / NW) + 31) & ~31;
-    const int lo = min(warp * per, L), hi = min(lo + per, L);
+    const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+    digit = __shfl_sync(0xffffffffu, d, src);
+    above = __shfl_sync(0xffffffffu, a, src);
+}
+
+// Asynchronous 16- and 8-byte global -> shared copies (cp.async), completed
+// together by cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void tk_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void tk_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+constexpr int kTkChunk = 32;   // kept rows per buffer of the gather (two buffers)
+
+// Shared space of topk_gather_kernel (one warp per block): the scores, two
+// buffers of kTkChunk kept rows (codes then (min, scale)), the histogram,
+// candidate keys and slots, the chosen candidates, the surely kept slots and
+// the merged kept list.
+template <int D>
+__host__ __device__ constexpr int tk_row_bytes() {
+    return D == 128 ? 80 : 48;   // d/2 code bytes + d/64 (min, scale) pairs, 16-byte multiple
+}
+template <int D>
+__host__ __device__ constexpr int tk_smem_bytes(int Lp, int kp) {
+    return 4 * Lp + 2 * kTkChunk * tk_row_bytes<D>() + 256 * 4 + 3 * kTkCand * 4 + 2 * 4 * kp;
+}
+
+// One warp: the ksel highest of the L scores sc[0..L) (shared; equal
+// scores: lower index first) as ascending indices sel[0..ksel).  mx / mn:
+// the scores' maximum and minimum.  Usual path: a histogram over 256 equal
+// bins of [mn, mx] gives the cut bin; every index in a higher bin is kept
+// (list a, ascending) and the cut bin's scores (at most kTkCand, in index
+// order) are ranked exactly, the chosen ones forming list b; the two lists
+// are merged by rank.  Otherwise (a crowded bin, or all scores equal) a radix
+// selection finds the cut key in four 8-bit digit passes and one pass in
+// index order keeps every key above it and the first `need` equal to it.
+__device__ void warp_topk_select(const float* sc, int L, int ksel, float mx, float mn, int* sel,
+                                 uint32_t* hist, uint32_t* ckey, int* cidx, int* lb, int* la,
+                                 int lane) {
     const uint32_t lt = (1u << lane) - 1u;
-    int gt_n = 0, eq_n = 0;
-    for (int c0 = lo; c0 < hi; c0 += 32) {
+    if (ksel >= L) {
+        for (int j = lane; j < L; j += 32) sel[j] = j;
+        __syncwarp();
+        return;
+    }
+    const float inv = 256.0f / (mx - mn);
+    if (mx > mn && inv < CUDART_INF_F) {
+        for (int i = lane; i < 256; i += 32) hist[i] = 0u;
+        __syncwarp();
+        for (int j = lane; j < L; j += 32) atomicAdd(&hist[tk_bin(sc[j], mn, inv)], 1u);
+        __syncwarp();
+        uint32_t bstar, above;
+        tk_scan(hist, static_cast<uint32_t>(ksel), lane, bstar, above);
+        const int need_b = ksel - static_cast<int>(above);   // kept from the cut bin, >= 1
+        // the surely kept (list a) and the cut bin's candidates, in index order
+        int na = 0, nc = 0;
+        for (int c0 = 0; c0 < L; c0 += 32) {
+            const int j = c0 + lane;
+            const float sj = j < L ? sc[j] : 0.0f;
+            const uint32_t bin = j < L ? tk_bin(sj, mn, inv) : 0u;
+            const bool sure = j < L && bin > bstar, cut = j < L && bin == bstar;
+            const unsigned bs = __ballot_sync(0xffffffffu, sure), bc = __ballot_sync(0xffffffffu, cut);
+            if (sure) la[na + __popc(bs & lt)] = j;
+            const int at = nc + __popc(bc & lt);
+            if (cut && at < kTkCand) {
+                ckey[at] = score_key(sj);
+                cidx[at] = j;
+            }
+            na += __popc(bs);
+            nc += __popc(bc);
+        }
+        __syncwarp();
+        if (nc <= kTkCand) {
+            // the need_b-th highest candidate key T, then the chosen ones in
+            // index order: keys above T, and the first (need_b - #above) equal
+            uint32_t t_key = 0u, t_gt = 0u;
+            bool has = false;
+            for (int i = lane; i < nc; i += 32) {
+                const uint32_t ki = ckey[i];
+                uint32_t gt = 0u, ge = 0u;
+                for (int m = 0; m < nc; ++m) {
+                    const uint32_t km = ckey[m];
+                    gt += km > ki;
+                    ge += km >= ki;
+                }
+                if (gt < static_cast<uint32_t>(need_b) && static_cast<uint32_t>(need_b) <= ge) {
+                    t_key = ki;
+                    t_gt = gt;
+                    has = true;
+                }
+            }
+            const int src = __ffs(__ballot_sync(0xffffffffu, has)) - 1;
+            const uint32_t T = __shfl_sync(0xffffffffu, t_key, src);
+            const int need_t = need_b - static_cast<int>(__shfl_sync(0xffffffffu, t_gt, src));
+            int nb = 0, eq_seen = 0;
+            for (int c0 = 0; c0 < nc; c0 += 32) {
+                const int i = c0 + lane;
+                const uint32_t k = i < nc ? ckey[i] : 0u;
+                const bool eq = i < nc && k == T;
+                const unsigned beq = __ballot_sync(0xffffffffu, eq);
+                const bool take = (i < nc && k > T) || (eq && eq_seen + __popc(beq & lt) < need_t);
+                const unsigned bt = __ballot_sync(0xffffffffu, take);
+                if (take) lb[nb + __popc(bt & lt)] = cidx[i];
+                nb += __popc(bt);
+                eq_seen += __popc(beq);
+            }
+            __syncwarp();
+            // merge the ascending lists a (na) and b (nb = need_b) by rank
+            auto rank = [](const int* list, int n, int x) {   // #elements < x
+                int lo = 0, hi = n;
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (list[mid] < x) lo = mid + 1; else hi = mid;
+                }
+                return lo;
+            };
+            for (int i = lane; i < na; i += 32) sel[i + rank(lb, nb, la[i])] = la[i];
+            for (int i = lane; i < nb; i += 32) sel[i + rank(la, na, lb[i])] = lb[i];
+            __syncwarp();
+            return;
+        }
+    }
+    // radix selection on the keys
+    uint32_t prefix = 0u, pmask = 0u, need = static_cast<uint32_t>(ksel);
+#pragma unroll 1
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = lane; i < 256; i += 32) hist[i] = 0u;
+        __syncwarp();
+        for (int j = lane; j < L; j += 32) {
+            const uint32_t k = score_key(sc[j]);
+            if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+        }
+        __syncwarp();
+        uint32_t dig, above;
+        tk_scan(hist, need, lane, dig, above);
+        __syncwarp();   // hist is cleared next
+        prefix |= dig << shift;
+        pmask |= 0xFFu << shift;
+        need -= above;
+    }
+    int at = 0, eq_seen = 0;
+    for (int c0 = 0; c0 < L; c0 += 32) {
         const int j = c0 + lane;
-        const uint32_t k = j < hi ? score_key(sc[j]) : 0u;
-        gt_n += __popc(__ballot_sync(0xffffffffu, j < hi && k > prefix));
-        eq_n += __popc(__ballot_sync(0xffffffffu, j < hi && k == prefix));
-    }
-    if (lane == 0) {
-        ws[5 + warp] = gt_n;
-        ws[5 + NW + warp] = eq_n;
-    }
-    __syncthreads();
-    int at = 0, eq_seen = 0;   // kept indices and equal keys of the warps before
-    for (int w = 0; w < warp; ++w) {
-        const int e = ws[5 + NW + w];
-        const int take_eq = min(e, max(static_cast<int>(need) - eq_seen, 0));
-        at += ws[5 + w] + take_eq;
-        eq_seen += e;
-    }
-    for (int c0 = lo; c0 < hi; c0 += 32) {
-        const int j = c0 + lane;
-        const uint32_t k = j < hi ? score_key(sc[j]) : 0u;
-        const bool eq = j < hi && k == prefix;
+        const uint32_t k = j < L ? score_key(sc[j]) : 0u;
+        const bool eq = j < L && k == prefix;
         const unsigned beq = __ballot_sync(0xffffffffu, eq);
-        const bool take = (j < hi && k > prefix) ||
+        const bool take = (j < L && k > prefix) ||
                           (eq && static_cast<uint32_t>(eq_seen + __popc(beq & lt)) < need);
         const unsigned bt = __ballot_sync(0xffffffffu, take);
         if (take) sel[at + __popc(bt & lt)] = j;
         at += __popc(bt);
         eq_seen += __popc(beq);
     }
-    __syncthreads();
-    return lsum;
+    __syncwarp();
 }
 
-// Pass 2 (the V sums) over nv keys read straight from global memory: key u
-// of the pass is cache row row0 + slot(u), slot(u) = u (dense) or sel[u]
-// (top-K, ascending), with weight p = sc[slot(u)] (dense: sc holds the
-// weights) or exp(sc[slot(u)] - mx) (top-K: sc holds the scores).  MMA e (nibble e of every
-// code word) has rows = dims (row g: word g, row g+8: word 8+g) and k = 16
-// keys paired in registers; B column n = g holds p * s_g (fp16) for group g.
-template <int D, bool TOPK>
-__device__ __forceinline__ void v_pass_global(const float* sc, float mx, const int* sel, int nv,
+// Top-K select-and-gather: one warp (the whole block) per (sequence, head)
+// u = blockIdx.x, over the scores and (max, min, normaliser) the scores pass
+// of the decode kernel wrote (sc_in [B*H][sc_ld], st_in [B*H][4]).  The
+// scores come into shared memory in one round of asynchronous copies; the
+// warp picks the kept slots (warp_topk_select); the kept rows' codes and
+// (min, scale) stream through two buffers of kTkChunk rows (the next chunk's
+// copies in flight while one is summed); out = sum_j p_j v^_j / normaliser
+// over them, p_j = exp(s_j - max), v^ = m + c s (unrounded, as the dense
+// kernels use it), lane l owning D/32 dimensions.  The V rows of the kept
+// slots are the only V bytes read.
+template <int D>
+__global__ void __launch_bounds__(32) topk_gather_kernel(
+    const float* __restrict__ sc_in, const float* __restrict__ st_in, int32_t sc_ld, int32_t H,
+    int32_t cap, int32_t pos, const int32_t* __restrict__ pad, int32_t keep_pct, int32_t kmax,
+    const uint8_t* __restrict__ v_codes, const float* __restrict__ v_meta,
+    __half* __restrict__ out, int32_t* __restrict__ sel_out) {
+    constexpr int G = D / 64, RB = D / 2, RS = tk_row_bytes<D>(), DPL = D / 32;
+    extern __shared__ __align__(128) uint8_t dyn[];
+    const int lane = threadIdx.x;
+    const int64_t u = blockIdx.x;
+    const int b = static_cast<int>(u / H), h = static_cast<int>(u % H);
+    const int p0 = pad ? min(max(pad[b], 0), pos) : 0;
+    const int L = pos + 1 - p0;
+    const int ksel = topk_count(L, keep_pct);
+    const int Lp = (pos + 4) & ~3, kp = (kmax + 3) & ~3;
+    float* sc = reinterpret_cast<float*>(dyn);
+    uint8_t* rows = dyn + 4 * Lp;
+    uint32_t* hist = reinterpret_cast<uint32_t*>(rows + 2 * kTkChunk * RS);
+    uint32_t* ckey = hist + 256;
+    int* cidx = reinterpret_cast<int*>(ckey + kTkCand);
+    int* lb = cidx + kTkCand;
+    int* la = lb + kTkCand;
+    int* sel = la + kp;
+    // the scores (sc_ld >= 4 * ceil(L / 4): whole 16-byte pieces stay in the row)
+    const float* g = sc_in + u * sc_ld;
+    for (int i = lane; 4 * i < L; i += 32) cp_async16(sc + 4 * i, g + 4 * i);
+    const float mx = st_in[u * 4], mn = st_in[u * 4 + 1], l = st_in[u * 4 + 2];
+    cp_async_wait_all();
+    __syncwarp();
+    warp_topk_select(sc, L, ksel, mx, mn, sel, hist, ckey, cidx, lb, la, lane);
+    if (sel_out)
+        for (int r = lane; r < kmax; r += 32) sel_out[u * kmax + r] = r < ksel ? p0 + sel[r] : -1;
+    // the kept rows' weights, into list a's space (no longer needed)
+    float* w = reinterpret_cast<float*>(la);
+    for (int r = lane; r < ksel; r += 32) w[r] = expf(sc[sel[r]] - mx);
+    // the kept rows, kTkChunk at a time: RB / 16 code pieces and the
+    // (min, scale) pairs per row
+    const int64_t row0 = u * cap + p0;
+    constexpr int CPR = RB / 16 + 1;
+    const int nch = (ksel + kTkChunk - 1) / kTkChunk;
+    auto issue = [&](int ci) {
+        const int r0 = ci * kTkChunk, n = min(kTkChunk, ksel - r0);
+        uint8_t* buf = rows + (ci & 1) * kTkChunk * RS;
+        for (int i = lane; i < n * CPR; i += 32) {
+            const int r = i / CPR, c = i % CPR;
+            const int64_t row = row0 + sel[r0 + r];
+            uint8_t* dst = buf + r * RS;
+            if (c < RB / 16)
+                cp_async16(dst + 16 * c, v_codes + row * RB + 16 * c);
+            else if (G == 2)
+                cp_async16(dst + RB, v_meta + row * 4);
+            else
+                cp_async8(dst + RB, v_meta + row * 2);
+        }
+        tk_commit();
+    };
+    const int grp = (lane * DPL) / 64;
+    float acc[DPL];
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) acc[i] = 0.0f;
+    issue(0);
+    for (int ci = 0; ci < nch; ++ci) {
+        if (ci + 1 < nch) {
+            issue(ci + 1);      // its buffer was last read by chunk ci - 1
+            tk_wait<1>();
+        } else {
+            tk_wait<0>();
+        }
+        __syncwarp();
+        const uint8_t* buf = rows + (ci & 1) * kTkChunk * RS;
+        const int r0 = ci * kTkChunk, n = min(kTkChunk, ksel - r0);
+#pragma unroll 4
+        for (int r = 0; r < n; ++r) {
+            const uint8_t* rr = buf + r * RS;
+            const float2 m = *reinterpret_cast<const float2*>(rr + RB + 8 * grp);
+            const uint32_t cw = DPL == 4 ? *reinterpret_cast<const uint16_t*>(rr + 2 * lane) : rr[lane];
+            const float wr = w[r0 + r];
+#pragma unroll
+            for (int i = 0; i < DPL; ++i)
+                acc[i] = fmaf(wr, fmaf(static_cast<float>((cw >> (4 * i)) & 15u), m.y, m.x), acc[i]);
+        }
+        __syncwarp();           // this buffer is refilled by chunk ci + 2
+    }
+    __half* o = out + u * D + lane * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; i += 2)
+        *reinterpret_cast<__half2*>(o + i) = __floats2half2_rn(acc[i] / l, acc[i + 1] / l);
+}
+
+// Pass 2 (the V sums) over the nv attended keys read straight from global
+// memory: key u is cache row row0 + u with weight p = sc[u].  MMA e (nibble e
+// of every code word) has rows = dims (row g: word g, row g+8: word 8+g) and
+// k = 16 keys paired in registers; B column n = g holds p * s_g (fp16) for
+// group g.
+template <int D>
+__device__ __forceinline__ void v_pass_global(const float* sc, int nv,
                                               const uint8_t* v_codes, const float* v_meta,
                                               int64_t row0, int warp, int g, int t,
                                               float (&accv)[8][4], float& s_pm) {
@@ -306,7 +424,7 @@ __device__ __forceinline__ void v_pass_global(const float* sc, float mx, const i
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int uu = min(keys[u], nv - 1);
-            slot[u] = TOPK ? sel[uu] : uu;
+            slot[u] = uu;
         }
         uint32_t bw[2] = {0u, 0u};
         {
@@ -314,7 +432,7 @@ __device__ __forceinline__ void v_pass_global(const float* sc, float mx, const i
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const bool ok = keys[u] < nv;
-                const float p = ok ? (TOPK ? expf(sc[slot[u]] - mx) : sc[slot[u]]) : 0.0f;
+                const float p = ok ? sc[slot[u]] : 0.0f;
                 float pv = 0.0f;
                 if (gown && ok) {
                     const float2 m = *reinterpret_cast<const float2*>(
@@ -355,21 +473,16 @@ __device__ __forceinline__ void v_pass_global(const float* sc, float mx, const i
     }
 }
 
-// Kept slots of one (sequence, head) to sel_out[0..kmax): p0 + sel[r] for
-// r < nv, -1 after.
-__device__ __forceinline__ void write_kept(int32_t* dst, const int* sel, int nv, int kmax, int p0) {
-    for (int r = threadIdx.x; r < kmax; r += kDecThreads) dst[r] = r < nv ? p0 + sel[r] : -1;
-}
-
-// TOPK: top-K sparse attention (keep_pct percent of the rows, the kept slots
-// optionally written to sel_out [B][H][kmax]); dynamic shared memory holds
-// the L scores, then (TOPK) kmax kept indices, the histogram and scratch.
-template <int D, bool TOPK>
+// SCORES: the scores pass of top-K attention -- no V pass; the L scores go
+// to sc_out[(b*H + h) * sc_ld ..] and (max, min, normaliser) to
+// st_out[(b*H + h) * 4 ..] for topk_gather_kernel.  Dynamic shared memory
+// holds the L scores.
+template <int D, bool SCORES>
 __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
     const __half* __restrict__ qkv, int64_t ld, int32_t H, int32_t cap, int32_t pos,
     const int32_t* __restrict__ pad, int32_t fuse_append, uint8_t* k_codes, uint8_t* v_codes,
-    float* k_meta, float* v_meta, __half* __restrict__ out, int32_t keep_pct, int32_t kmax,
-    int32_t* __restrict__ sel_out) {
+    float* k_meta, float* v_meta, __half* __restrict__ out, float* __restrict__ sc_out,
+    float* __restrict__ st_out, int32_t sc_ld) {
     constexpr int G = D / 64;            // groups per head row
     constexpr int RB = D / 2;            // code bytes per row
     constexpr int WPT = D / 32;          // code words per lane per row in pass 1
@@ -468,7 +581,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
     const int ntile = (L + 15) >> 4;
 
     // ---------------- pass 1: scores
-    float lmax = -CUDART_INF_F, lmin = CUDART_INF_F;   // lmin: TOPK only
+    float lmax = -CUDART_INF_F, lmin = CUDART_INF_F;   // lmin: SCORES only
     for (int kt = warp; kt < ntile; kt += NWARP) {
         const int ja = min(kt * 16 + g, L - 1), jb = min(kt * 16 + g + 8, L - 1);
         const uint8_t* ra = k_codes + (row0 + ja) * RB + t * (WPT * 4);
@@ -521,42 +634,30 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
                     const float s = dot * attn_scale;
                     sc[j] = s;
                     lmax = fmaxf(lmax, s);
-                    if (TOPK) lmin = fminf(lmin, s);
+                    if (SCORES) lmin = fminf(lmin, s);
                 }
             }
         }
     }
     lmax = warp_max(lmax);
     if (lane == 0) red[warp] = lmax;
-    if (TOPK) {
+    if (SCORES) {
         lmin = -warp_max(-lmin);
         if (lane == 0) red_min[warp] = lmin;
     }
     __syncthreads();
-    float mx = red[0], mn = TOPK ? red_min[0] : 0.0f;
+    float mx = red[0], mn = SCORES ? red_min[0] : 0.0f;
 #pragma unroll
     for (int i = 1; i < NWARP; ++i) {
         mx = fmaxf(mx, red[i]);
-        if (TOPK) mn = fminf(mn, red_min[i]);
+        if (SCORES) mn = fminf(mn, red_min[i]);
     }
     __syncthreads();
-    int nv = L;            // keys of pass 2
-    int* sel = nullptr;    // TOPK: their slots (offsets from p0), ascending
     float lsum = 0.0f;
-    if constexpr (TOPK) {
-        // the scores stay in sc (pass 2 takes exp of the kept ones)
-        const int Lp = (pos + 4) & ~3;   // the scores' space, for the largest L
-        sel = reinterpret_cast<int*>(dsm + Lp);
-        nv = topk_count(L, keep_pct);
-        lsum = topk_select(sc, L, nv, mx, mn, sel,
-                           reinterpret_cast<uint8_t*>(sel + ((kmax + 3) & ~3)));
-        if (sel_out) write_kept(sel_out + (static_cast<int64_t>(b) * H + h) * kmax, sel, nv, kmax, p0);
-    } else {
-        for (int j = threadIdx.x; j < L; j += kDecThreads) {
-            const float p = expf(sc[j] - mx);
-            sc[j] = p;
-            lsum += p;
-        }
+    for (int j = threadIdx.x; j < L; j += kDecThreads) {
+        const float p = expf(sc[j] - mx);
+        if (!SCORES) sc[j] = p;   // the scores pass keeps the scores
+        lsum += p;
     }
     lsum = warp_sum(lsum);
     if (lane == 0) red[warp] = lsum;
@@ -564,14 +665,24 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
     float l = 0.0f;
 #pragma unroll
     for (int i = 0; i < NWARP; ++i) l += red[i];
+    if constexpr (SCORES) {
+        const int64_t bh = static_cast<int64_t>(b) * H + h;
+        for (int j = threadIdx.x; j < L; j += kDecThreads) sc_out[bh * sc_ld + j] = sc[j];
+        if (threadIdx.x == 0) {
+            st_out[bh * 4] = mx;
+            st_out[bh * 4 + 1] = mn;
+            st_out[bh * 4 + 2] = l;
+        }
+        return;
+    }
 
-    // ---------------- pass 2: V (all L rows, or the kept ones)
+    // ---------------- pass 2: V
     float accv[8][4];
 #pragma unroll
     for (int e = 0; e < 8; ++e) accv[e][0] = accv[e][1] = accv[e][2] = accv[e][3] = 0.0f;
     float s_pm = 0.0f;   // this lane's keys: sum p * min (group g)
     const bool gown = g < G;
-    v_pass_global<D, TOPK>(sc, mx, sel, nv, v_codes, v_meta, row0, warp, g, t, accv, s_pm);
+    v_pass_global<D>(sc, L, v_codes, v_meta, row0, warp, g, t, accv, s_pm);
     // group sums of this warp: reduce over the 4 lanes (g, t) of each group
 #pragma unroll
     for (int o = 1; o < 4; o <<= 1) s_pm += __shfl_xor_sync(0xffffffffu, s_pm, o);
@@ -621,20 +732,18 @@ constexpr int kRB128 = 64;         // code bytes per row (d = 128)
 constexpr int kMB128 = 16;         // (min, scale) bytes per row (2 groups)
 constexpr int kChunkBytes = kCKMax * (kRB128 + kMB128);   // codes, then meta
 
-// TOPK: top-K sparse attention.  Only the K chunks are staged; after pass 1
-// the idle ring holds the selection's histogram, scratch and kept indices
-// (after the scores instead when kmax is too large for it), and pass 2
-// gathers the kept V rows straight from global memory.
-__host__ __device__ constexpr bool topk_in_ring(int kmax) {
-    return kTkScratchBytes + 4 * ((kmax + 3) & ~3) <= kNB * kChunkBytes;
-}
+// SCORES: the scores pass of top-K attention.  Only the K chunks are
+// staged; after pass 1 the scores go to sc_out[(b*H + h) * sc_ld ..] and
+// (max, min, normaliser) to st_out[(b*H + h) * 4 ..] for topk_gather_kernel,
+// and there is no V pass.
 
-template <bool TOPK>
+template <bool SCORES>
 __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_kernel(
     const __half* __restrict__ qkv, int64_t ld, int32_t H, int32_t cap, int32_t pos,
     const int32_t* __restrict__ pad, int32_t fuse_append, uint8_t* k_codes, uint8_t* v_codes,
     float* k_meta, float* v_meta, __half* __restrict__ out, int* status,
-    unsigned long long wait_ns, int32_t keep_pct, int32_t kmax, int32_t* __restrict__ sel_out) {
+    unsigned long long wait_ns, float* __restrict__ sc_out, float* __restrict__ st_out,
+    int32_t sc_ld) {
     constexpr int D = 128, G = 2, RB = kRB128, WPT = D / 32, NX = 2 * WPT;
     constexpr int NWARP = kDecThreads / 32;
     extern __shared__ __align__(128) uint8_t dyn[];
@@ -653,7 +762,7 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     // chunks of kCK keys; a remainder of <= 16 keys joins the last full chunk
     int nK = (L + kCK - 1) / kCK;
     if (nK > 1 && L - (nK - 1) * kCK <= 16) --nK;
-    const int nseq = TOPK ? nK : 2 * nK;   // K chunks, then (dense) V chunks
+    const int nseq = SCORES ? nK : 2 * nK;   // K chunks, then (dense) V chunks
     auto chunk_n = [&](int c) { return c == nK - 1 ? L - c * kCK : kCK; };
     const int64_t h1 = static_cast<int64_t>(H) * D;
     const int64_t rowb = (static_cast<int64_t>(b) * H + h) * cap;  // cache row of slot 0
@@ -767,7 +876,7 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     const float Q0 = qsum[0], Q1 = qsum[1];
 
     // ---------------- pass 1: scores
-    float lmax = -CUDART_INF_F, lmin = CUDART_INF_F;   // lmin: TOPK only
+    float lmax = -CUDART_INF_F, lmin = CUDART_INF_F;   // lmin: SCORES only
     for (int c = 0; c < nK; ++c) {
         const bool ok = wait_chunk(c);
         const uint8_t* buf = dyn + (c % kNB) * kChunkBytes;
@@ -807,7 +916,7 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
                         const float s = dot * attn_scale;
                         sc[r0 + jl] = s;
                         lmax = fmaxf(lmax, s);
-                        if (TOPK) lmin = fminf(lmin, s);
+                        if (SCORES) lmin = fminf(lmin, s);
                     }
                 }
             }
@@ -821,36 +930,23 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     }
     lmax = warp_max(lmax);
     if (lane == 0) red[warp] = lmax;
-    if (TOPK) {
+    if (SCORES) {
         lmin = -warp_max(-lmin);
         if (lane == 0) red_min[warp] = lmin;
     }
     __syncthreads();
-    float mx = red[0], mn = TOPK ? red_min[0] : 0.0f;
+    float mx = red[0], mn = SCORES ? red_min[0] : 0.0f;
 #pragma unroll
     for (int i = 1; i < NWARP; ++i) {
         mx = fmaxf(mx, red[i]);
-        if (TOPK) mn = fminf(mn, red_min[i]);
+        if (SCORES) mn = fminf(mn, red_min[i]);
     }
     __syncthreads();
-    int nv = L;            // TOPK: kept keys
-    int* sel = nullptr;    // TOPK: their slots (offsets from p0), ascending
     float lsum = 0.0f;
-    if constexpr (TOPK) {
-        if (!failed) {     // block-uniform; no chunk is in flight after a clean pass 1
-            // scratch, then the kept list: in the idle ring, or after the scores
-            uint8_t* x = topk_in_ring(kmax) ? dyn
-                                            : dyn + kNB * kChunkBytes + 4 * ((pos + 4) & ~3);
-            sel = reinterpret_cast<int*>(x + kTkScratchBytes);
-            nv = topk_count(L, keep_pct);
-            lsum = topk_select(sc, L, nv, mx, mn, sel, x);   // the scores stay in sc
-            if (sel_out) write_kept(sel_out + (static_cast<int64_t>(b) * H + h) * kmax, sel, nv, kmax, p0);
-        }
-    }
-    if (!TOPK && !failed) {
+    if (!failed) {
         for (int j = threadIdx.x; j < L; j += kDecThreads) {
             const float p = expf(sc[j] - mx);
-            sc[j] = p;
+            if (!SCORES) sc[j] = p;   // the scores pass keeps the scores
             lsum += p;
         }
     }
@@ -860,6 +956,16 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     float l = 0.0f;
 #pragma unroll
     for (int i = 0; i < NWARP; ++i) l += red[i];
+    if (SCORES && !failed) {   // block-uniform; no chunk is in flight after a clean pass 1
+        const int64_t bh = static_cast<int64_t>(b) * H + h;
+        for (int j = threadIdx.x; j < L; j += kDecThreads) sc_out[bh * sc_ld + j] = sc[j];
+        if (threadIdx.x == 0) {
+            st_out[bh * 4] = mx;
+            st_out[bh * 4 + 1] = mn;
+            st_out[bh * 4 + 2] = l;
+        }
+        return;
+    }
 
     // ---------------- pass 2: V (see decode_attn_kernel for the MMA layout)
     float accv[8][4];
@@ -867,8 +973,7 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     for (int e = 0; e < 8; ++e) accv[e][0] = accv[e][1] = accv[e][2] = accv[e][3] = 0.0f;
     float s_pm = 0.0f;   // this lane's keys: sum p * min (group g)
     const bool gown = g < G;
-    if (TOPK && !failed) v_pass_global<D, true>(sc, mx, sel, nv, v_codes, v_meta, row0, warp, g, t, accv, s_pm);
-    for (int c = 0; c < nK && !failed && !TOPK; ++c) {
+    for (int c = 0; c < nK && !failed && !SCORES; ++c) {
         const int seq = nK + c;
         const bool ok = wait_chunk(seq);
         const uint8_t* buf = dyn + (seq % kNB) * kChunkBytes;
@@ -1183,17 +1288,34 @@ double decode_attn_bytes(int D, double bh, int L, int nv, bool fuse_append) {
     return bh * ((static_cast<double>(L) + nv) * row + (fuse_append ? 2.0 * row : 0.0) + 3.0 * D * 2 + D * 2);
 }
 
-template <int D, bool TOPK>
+// Scores workspace of top-K attention: sc [B*H][ld] fp32 (ld = the largest
+// L rounded up to 4), then st [B*H][4] fp32 (max, min, normaliser).
+struct TopkWs {
+    float* sc;
+    float* st;
+    int sc_ld;
+    size_t bytes;
+};
+TopkWs topk_ws_layout(int32_t B, int32_t H, int32_t pos, void* base) {
+    TopkWs w{};
+    w.sc_ld = (pos + 4) & ~3;
+    const size_t a = (static_cast<size_t>(B) * H * w.sc_ld * 4 + 255) & ~static_cast<size_t>(255);
+    w.bytes = a + ((static_cast<size_t>(B) * H * 16 + 255) & ~static_cast<size_t>(255));
+    w.sc = static_cast<float*>(base);
+    w.st = base ? reinterpret_cast<float*>(static_cast<char*>(base) + a) : nullptr;
+    return w;
+}
+
+template <int D, bool SCORES>
 fg_status launch_decode_t(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
-                          const int32_t* pad, int32_t fuse_append, int32_t keep_pct, int32_t kmax,
-                          int32_t* sel_out, __half* out, cudaStream_t st) {
+                          const int32_t* pad, int32_t fuse_append, __half* out, const TopkWs& w,
+                          cudaStream_t st) {
     const int L = pos + 1;
-    size_t smem = sizeof(float) * ((L + 3) & ~3);
-    if (TOPK) smem += 4 * static_cast<size_t>((kmax + 3) & ~3) + kTkScratchBytes;
+    const size_t smem = sizeof(float) * ((L + 3) & ~3);
     if (smem > kMaxDynSmem)
-        return fg::set_error(FG_ERR_UNSUPPORTED, "decode_attn: context %d at keep %d%% needs %zu B of shared memory",
-                             L, TOPK ? keep_pct : 100, smem);
-    auto kern = decode_attn_kernel<D, TOPK>;
+        return fg::set_error(FG_ERR_UNSUPPORTED, "decode_attn: context %d needs %zu B of shared memory",
+                             L, smem);
+    auto kern = decode_attn_kernel<D, SCORES>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
@@ -1201,39 +1323,63 @@ fg_status launch_decode_t(const __half* qkv, int64_t ld, const fg_kv4* c, int32_
     }
     dim3 grid(c->H, c->B);
     const double bh = static_cast<double>(c->B) * c->H;
-    fg::TraceScope ts(FG_TRACE_ATTN_DECODE, st, 4.0 * bh * L * D,
-                      decode_attn_bytes(D, bh, L, TOPK ? kmax : L, fuse_append != 0));
+    fg::TraceScope ts(FG_TRACE_ATTN_DECODE, st, (SCORES ? 2.0 : 4.0) * bh * L * D,
+                      decode_attn_bytes(D, bh, L, SCORES ? 0 : L, fuse_append != 0));
     kern<<<grid, kDecThreads, smem, st>>>(qkv, ld, c->H, c->cap, pos, pad, fuse_append,
                                           c->k_codes, c->v_codes, c->k_meta, c->v_meta, out,
-                                          keep_pct, kmax, sel_out);
+                                          w.sc, w.st, w.sc_ld);
     return fg::cuda_error(cudaGetLastError(), "decode_attn launch");
 }
 
-template <bool TOPK>
+template <bool SCORES>
 fg_status launch_decode_staged(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
-                               const int32_t* pad, int32_t fuse_append, int32_t keep_pct,
-                               int32_t kmax, int32_t* sel_out, __half* out, cudaStream_t st) {
+                               const int32_t* pad, int32_t fuse_append, __half* out,
+                               const TopkWs& w, cudaStream_t st) {
     constexpr int D = 128;
     const int L = pos + 1;
-    size_t smem = static_cast<size_t>(kNB) * kChunkBytes + sizeof(float) * ((L + 3) & ~3);
-    if (TOPK && !topk_in_ring(kmax))
-        smem += 4 * static_cast<size_t>((kmax + 3) & ~3) + kTkScratchBytes;
+    const size_t smem = static_cast<size_t>(kNB) * kChunkBytes + sizeof(float) * ((L + 3) & ~3);
     if (smem > kMaxDynSmem)
-        return fg::set_error(FG_ERR_UNSUPPORTED, "decode_attn: context %d at keep %d%% needs %zu B of shared memory",
-                             L, TOPK ? keep_pct : 100, smem);
-    auto kern = decode_attn_staged_kernel<TOPK>;
+        return fg::set_error(FG_ERR_UNSUPPORTED, "decode_attn: context %d needs %zu B of shared memory",
+                             L, smem);
+    auto kern = decode_attn_staged_kernel<SCORES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return fg::cuda_error(e, "decode_attn smem attribute");
     dim3 grid(c->H, c->B);
     const double bh = static_cast<double>(c->B) * c->H;
-    fg::TraceScope ts(FG_TRACE_ATTN_DECODE, st, 4.0 * bh * L * D,
-                      decode_attn_bytes(D, bh, L, TOPK ? kmax : L, fuse_append != 0));
+    fg::TraceScope ts(FG_TRACE_ATTN_DECODE, st, (SCORES ? 2.0 : 4.0) * bh * L * D,
+                      decode_attn_bytes(D, bh, L, SCORES ? 0 : L, fuse_append != 0));
     kern<<<grid, kDecThreads, smem, st>>>(qkv, ld, c->H, c->cap, pos, pad, fuse_append,
                                           c->k_codes, c->v_codes, c->k_meta, c->v_meta, out,
-                                          fg::device_status_ptr(), fg::wait_limit_ns(), keep_pct,
-                                          kmax, sel_out);
+                                          fg::device_status_ptr(), fg::wait_limit_ns(), w.sc, w.st,
+                                          w.sc_ld);
     return fg::cuda_error(cudaGetLastError(), "decode_attn launch");
+}
+
+template <int D>
+fg_status launch_topk_gather(const fg_kv4* c, int32_t pos, const int32_t* pad, int32_t keep_pct,
+                             int32_t kmax, int32_t* sel_out, __half* out, const TopkWs& w,
+                             cudaStream_t st) {
+    const int Lp = (pos + 4) & ~3, kp = (kmax + 3) & ~3;
+    const size_t smem = static_cast<size_t>(tk_smem_bytes<D>(Lp, kp));
+    if (smem > kMaxDynSmem)
+        return fg::set_error(FG_ERR_UNSUPPORTED,
+                             "decode_attn_topk: context %d at keep %d%% needs %zu B of shared memory",
+                             pos + 1, keep_pct, smem);
+    auto kern = topk_gather_kernel<D>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return fg::cuda_error(e, "topk_gather smem attribute");
+    }
+    const int64_t units = static_cast<int64_t>(c->B) * c->H;
+    const double row = D / 2 + (D / 64) * 8.0;
+    fg::TraceScope ts(FG_TRACE_ATTN_DECODE, st, 2.0 * units * kmax * D,
+                      static_cast<double>(units) * (kmax * row + D * 2.0));
+    kern<<<static_cast<unsigned>(units), 32, smem, st>>>(w.sc, w.st, w.sc_ld, c->H, c->cap, pos, pad,
+                                                          keep_pct, kmax, c->v_codes, c->v_meta,
+                                                          out, sel_out);
+    return fg::cuda_error(cudaGetLastError(), "topk_gather launch");
 }
 
 }  // namespace
@@ -1241,22 +1387,37 @@ fg_status launch_decode_staged(const __half* qkv, int64_t ld, const fg_kv4* c, i
 namespace fg {
 
 fg_status launch_decode_attn(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
-                             const int32_t* pad, int32_t fuse_append, int32_t keep_pct,
-                             int32_t* sel_out, __half* out, cudaStream_t st) {
+                             const int32_t* pad, int32_t fuse_append, __half* out,
+                             cudaStream_t st) {
     if (c->B == 0) return FG_OK;
-    // dense unless rows are dropped or the kept slots are asked for
-    const bool topk = sel_out != nullptr || (keep_pct > 0 && keep_pct < 100);
-    const int32_t pct = (keep_pct > 0 && keep_pct < 100) ? keep_pct : 100;
-    const int32_t kmax = topk ? topk_count_host(pos + 1, pct) : 0;
-    if (c->d == 64)
-        return topk ? launch_decode_t<64, true>(qkv, ld, c, pos, pad, fuse_append, pct, kmax, sel_out, out, st)
-                    : launch_decode_t<64, false>(qkv, ld, c, pos, pad, fuse_append, 0, 0, nullptr, out, st);
-    return topk ? launch_decode_staged<true>(qkv, ld, c, pos, pad, fuse_append, pct, kmax, sel_out, out, st)
-                : launch_decode_staged<false>(qkv, ld, c, pos, pad, fuse_append, 0, 0, nullptr, out, st);
+    const TopkWs none{};
+    if (c->d == 64) return launch_decode_t<64, false>(qkv, ld, c, pos, pad, fuse_append, out, none, st);
+    return launch_decode_staged<false>(qkv, ld, c, pos, pad, fuse_append, out, none, st);
+}
+
+size_t decode_topk_ws_bytes(int32_t B, int32_t H, int32_t pos) {
+    return topk_ws_layout(B, H, pos, nullptr).bytes;
 }
 
 int32_t decode_topk_kmax(int32_t pos, int32_t keep_pct) {
-    return topk_count_host(pos + 1, (keep_pct > 0 && keep_pct < 100) ? keep_pct : 100);
+    return topk_count_host(pos + 1, keep_pct);
+}
+
+fg_status launch_decode_attn_topk(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
+                                  const int32_t* pad, int32_t fuse_append, int32_t keep_pct,
+                                  int32_t* sel_out, void* ws, size_t ws_bytes, __half* out,
+                                  cudaStream_t st) {
+    if (c->B == 0) return FG_OK;
+    const TopkWs w = topk_ws_layout(c->B, c->H, pos, ws);
+    if (ws == nullptr || ws_bytes < w.bytes)
+        return set_error(FG_ERR_WORKSPACE, "decode_attn_topk: workspace %zu < %zu bytes", ws_bytes,
+                         w.bytes);
+    const int32_t kmax = decode_topk_kmax(pos, keep_pct);
+    fg_status s = c->d == 64 ? launch_decode_t<64, true>(qkv, ld, c, pos, pad, fuse_append, out, w, st)
+                             : launch_decode_staged<true>(qkv, ld, c, pos, pad, fuse_append, out, w, st);
+    if (s != FG_OK) return s;
+    return c->d == 64 ? launch_topk_gather<64>(c, pos, pad, keep_pct, kmax, sel_out, out, w, st)
+                      : launch_topk_gather<128>(c, pos, pad, keep_pct, kmax, sel_out, out, w, st);
 }
 
 fg_status launch_prefill_attn(const __half* qkv, int32_t B, int32_t s, int32_t H, int32_t d,

@@ -60,12 +60,18 @@ fg_status launch_embed(const int32_t* ids, int64_t ntok, int32_t T, int32_t pos0
                        const int32_t* pad, const __half* e_tok, const __half* e_pos, int32_t h1,
                        __half* y, cudaStream_t st);
 fg_status launch_argmax(const float* logits, int64_t B, int64_t V, int32_t* out, cudaStream_t st);
-// keep_pct 0 or 100 with sel_out NULL: dense attention; otherwise top-K
-// sparse attention keeping ceil(L * keep_pct / 100) rows (keep_pct 0 read as
-// 100), the kept slots written to sel_out [B][H][decode_topk_kmax] if given.
 fg_status launch_decode_attn(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
-                             const int32_t* pad, int32_t fuse_append, int32_t keep_pct,
-                             int32_t* sel_out, __half* out, cudaStream_t st);
+                             const int32_t* pad, int32_t fuse_append, __half* out,
+                             cudaStream_t st);
+// Top-K sparse attention keeping ceil(L * keep_pct / 100) rows (1 <= keep_pct
+// <= 100): a scores pass then a select-and-gather pass, through a workspace
+// of decode_topk_ws_bytes(B, H, pos); the kept slots are written to sel_out
+// [B][H][decode_topk_kmax] if given.
+fg_status launch_decode_attn_topk(const __half* qkv, int64_t ld, const fg_kv4* c, int32_t pos,
+                                  const int32_t* pad, int32_t fuse_append, int32_t keep_pct,
+                                  int32_t* sel_out, void* ws, size_t ws_bytes, __half* out,
+                                  cudaStream_t st);
+size_t decode_topk_ws_bytes(int32_t B, int32_t H, int32_t pos);
 int32_t decode_topk_kmax(int32_t pos, int32_t keep_pct);
 // The uncompressed (fp16) cache: store of T rows per sequence at slot0, and
 // decode attention with the append fused.

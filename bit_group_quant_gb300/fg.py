@@ -29,7 +29,8 @@ EXPORTS = (
     "fg_gemm_f16_f32out", "fg_layernorm", "fg_embed", "fg_kv_append_g4",
     "fg_decode_attn_g4", "fg_prefill_attn", "fg_layer_workspace_bytes", "fg_layer_step",
     "fg_debug_set", "fg_trace_begin", "fg_trace_end", "fg_dequant_gemm_g4_noalloc",
-    "fg_argmax", "fg_decode_attn_topk_g4", "fg_topk_count", "fg_kv_store_f16",
+    "fg_argmax", "fg_decode_attn_topk_g4", "fg_decode_attn_topk_workspace_bytes",
+    "fg_topk_count", "fg_kv_store_f16",
     "fg_decode_attn_f16", "fg_layer_step_kv16",
 )
 
@@ -114,15 +115,17 @@ def load(path: str = LIB_PATH):
             "fg_argmax": ([P, I64, I64, P, P], st),
             "fg_kv_append_g4": ([P, I64, ctypes.POINTER(c_kv4), I32, P], st),
             "fg_decode_attn_g4": ([P, I64, ctypes.POINTER(c_kv4), I32, P, I32, P, P], st),
-            "fg_decode_attn_topk_g4": ([P, I64, ctypes.POINTER(c_kv4), I32, P, I32, I32, P, P, P],
-                                       st),
+            "fg_decode_attn_topk_g4": ([P, I64, ctypes.POINTER(c_kv4), I32, P, I32, I32, P, P, P,
+                                        SZ, P], st),
+            "fg_decode_attn_topk_workspace_bytes": ([I32, I32, I32], SZ),
             "fg_topk_count": ([I32, I32], I32),
             "fg_kv_store_f16": ([P, I64, I32, ctypes.POINTER(c_kv16), I32, P], st),
             "fg_decode_attn_f16": ([P, I64, ctypes.POINTER(c_kv16), I32, P, I32, P, P], st),
             "fg_layer_step_kv16": ([ctypes.POINTER(c_layer), ctypes.POINTER(c_kv16), P, P, I32,
                                     I32, I32, P, c_policy, P, SZ, P], st),
             "fg_prefill_attn": ([P, I32, I32, I32, I32, P, ctypes.POINTER(c_kv4), P, P], st),
-            "fg_layer_workspace_bytes": ([ctypes.POINTER(c_layer), I32, I32, I32, c_policy], SZ),
+            "fg_layer_workspace_bytes": ([ctypes.POINTER(c_layer), I32, I32, I32, I32, c_policy],
+                                         SZ),
             "fg_layer_step": ([ctypes.POINTER(c_layer), ctypes.POINTER(c_kv4), P, P, I32, I32,
                                I32, P, c_policy, P, SZ, P], st),
             "fg_debug_set": ([I32, I64], st),
@@ -396,10 +399,19 @@ def fg_topk_count(n, keep_pct) -> int:
     return int(load().fg_topk_count(int(n), int(keep_pct)))
 
 
+def fg_decode_attn_topk_workspace_bytes(B, H, pos) -> int:
+    return int(load().fg_decode_attn_topk_workspace_bytes(int(B), int(H), int(pos)))
+
+
 def fg_decode_attn_topk_g4(qkv, cache: KV4, pos, keep_pct, fuse_append=True, out=None,
-                           sel_out=None, stream=None, pad=None):
+                           sel_out=None, stream=None, pad=None, workspace=None):
     """sel_out: None, True (allocate [B][H][kmax] int32 and return it), or a
-    device int32 tensor of that shape.  Returns out, or (out, sel_out)."""
+    device int32 tensor of that shape.  workspace: None (allocated here) or
+    a uint8 device tensor of fg_decode_attn_topk_workspace_bytes.  Returns
+    out, or (out, sel_out)."""
+    if workspace is None:
+        n = fg_decode_attn_topk_workspace_bytes(cache.B, cache.H, pos)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=qkv.device)
     if out is None:
         out = torch.empty((qkv.shape[0], cache.H * cache.d), dtype=torch.float16,
                           device=qkv.device)
@@ -412,6 +424,8 @@ def fg_decode_attn_topk_g4(qkv, cache: KV4, pos, keep_pct, fuse_append=True, out
     _ok(load().fg_decode_attn_topk_g4(_ptr(qkv), qkv.shape[1], ctypes.byref(c), int(pos),
                                       _pad(pad, cache.B), int(keep_pct), 1 if fuse_append else 0,
                                       _ptr(out), _ptr(sel_out) if want else None,
+                                      _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(),
                                       _stream(stream)))
     return (out, sel_out) if want else out
 
@@ -425,9 +439,10 @@ def fg_prefill_attn(qkv, B, s, H, d, cache: KV4 | None = None, out=None, stream=
     return out
 
 
-def fg_layer_workspace_bytes(layer_c: c_layer, phase, bls, T, policy: c_policy) -> int:
+def fg_layer_workspace_bytes(layer_c: c_layer, phase, bls, T, policy: c_policy, cap=0) -> int:
+    """cap: the cache capacity (sizes top-K attention's scores; 0 otherwise)."""
     return int(load().fg_layer_workspace_bytes(ctypes.byref(layer_c), int(phase), int(bls),
-                                               int(T), policy))
+                                               int(T), int(cap), policy))
 
 
 def fg_kv_store_f16(qkv, T, cache: KV16, slot0=0, stream=None):

@@ -112,10 +112,10 @@ class LayerStack:
         return fg.c_policy(self.gbs, self.k, order_code, self.topk_pct)
 
     def workspace(self, phase, T, order_code):
-        key = (phase, T, order_code != fg.FG_ORDER_BLOCK)
+        key = (phase, T, order_code != fg.FG_ORDER_BLOCK, self.topk_pct)
         if key not in self._ws:
             n = fg.fg_layer_workspace_bytes(self.c_layers[0], phase, self.bls, T,
-                                            self.policy(order_code))
+                                            self.policy(order_code), cap=self.cap)
             self._ws[key] = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
         return self._ws[key]
 
@@ -329,10 +329,10 @@ class HostLayerStack(LayerStack):
         self.fetched[slot].record(cp)
 
     def workspace(self, phase, T, order_code):
-        key = (phase, T, order_code != fg.FG_ORDER_BLOCK)
+        key = (phase, T, order_code != fg.FG_ORDER_BLOCK, self.topk_pct)
         if key not in self._ws:
             n = fg.fg_layer_workspace_bytes(self.c_slot[0][0], phase, self.bls, T,
-                                            self.policy(order_code))
+                                            self.policy(order_code), cap=self.cap)
             self._ws[key] = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
         return self._ws[key]
 

@@ -116,7 +116,8 @@ typedef struct fg_kv16 {
 enum { FG_ORDER_BLOCK = 0, FG_ORDER_BATCHES = 1, FG_ORDER_BATCHES_REV = 2 };
 /* topk_pct: 0 (or 100) for dense decode attention; 1..99 runs each decode
  * step's attention as fg_decode_attn_topk_g4 at that percentage (the prefill
- * stays dense).  (ABI 3.0 added this field.) */
+ * stays dense; the layer workspace then holds the scores).  (ABI 3.0 added
+ * this field.) */
 typedef struct fg_policy {
     int32_t gbs;
     int32_t k;
@@ -285,19 +286,31 @@ fg_status fg_decode_attn_g4(const fg_f16* qkv, int64_t qkv_ld,
  * with the highest fp32 scores (equal scores: lower slot first); and
  * out = sum_{j in S} p_j v^_j -- rows outside S add nothing, the weights are
  * not renormalised over S.  Only the V rows of S are read from memory.
- * keep_pct in [1, 100]; 100 keeps every row and gives bit for bit the output
- * of fg_decode_attn_g4.  sel_out: NULL, or device [B][H][kmax] int32 with
- * kmax = fg_topk_count(pos + 1, keep_pct), receiving each (b, h)'s kept slots
- * ascending, -1 after its own count.  Other arguments, layouts and fusion as
- * for fg_decode_attn_g4.  Errors: FG_ERR_SHAPE for keep_pct outside [1, 100];
- * FG_ERR_ALIGN if pad or sel_out is not 4-byte aligned; FG_ERR_UNSUPPORTED
- * if the context's scores and kept list exceed a block's shared memory
- * (about 27,000 slots at keep_pct 100). */
+ * Two launches: a scores pass over K (the append fused) writes every score
+ * to the workspace, then one warp per (b, h) selects and gathers.
+ * keep_pct in [1, 100]; 100 keeps every row (the result then agrees with
+ * fg_decode_attn_g4 within rounding).  sel_out: NULL, or device
+ * [B][H][kmax] int32 with kmax = fg_topk_count(pos + 1, keep_pct),
+ * receiving each (b, h)'s kept slots ascending, -1 after its own count.
+ * workspace: device scratch of at least
+ * fg_decode_attn_topk_workspace_bytes(B, H, pos) bytes, 256-byte aligned,
+ * owned by the caller.  Other arguments, layouts and fusion as for
+ * fg_decode_attn_g4.  Errors: FG_ERR_SHAPE for keep_pct outside [1, 100];
+ * FG_ERR_ALIGN if pad or sel_out is not 4-byte aligned or the workspace
+ * not 256-byte aligned; FG_ERR_WORKSPACE if it is missing or too small;
+ * FG_ERR_UNSUPPORTED if the kept list exceeds the selecting warps' shared
+ * memory (more than about 6,600 kept slots). */
+size_t fg_decode_attn_topk_workspace_bytes(int32_t B, int32_t H, int32_t pos);
 fg_status fg_decode_attn_topk_g4(const fg_f16* qkv, int64_t qkv_ld,
                                  const fg_kv4* cache, int32_t pos,
                                  const int32_t* pad, int32_t keep_pct,
                                  int32_t fuse_append, fg_f16* out,
-                                 int32_t* sel_out, fg_stream stream);
+                                 int32_t* sel_out, void* workspace,
+                                 size_t ws_bytes, fg_stream stream);
+
+/* Rows kept by top-K attention out of n: ceil(n * keep_pct / 100) (at least
+ * one for n >= 1).  Returns -1 for n < 0 or keep_pct outside [1, 100]. */
+int32_t fg_topk_count(int32_t n, int32_t keep_pct);
 
 /* Store rows of k and v into the fp16 cache: token t (0 <= t < T) of
  * sequence b, row b*T + t of qkv ([B*T][qkv_ld] fp16 holding q | k | v of
@@ -320,10 +333,6 @@ fg_status fg_decode_attn_f16(const fg_f16* qkv, int64_t qkv_ld,
                              const fg_kv16* cache, int32_t pos,
                              const int32_t* pad, int32_t fuse_append,
                              fg_f16* out, fg_stream stream);
-
-/* Rows kept by top-K attention out of n: ceil(n * keep_pct / 100) (at least
- * one for n >= 1).  Returns -1 for n < 0 or keep_pct outside [1, 100]. */
-int32_t fg_topk_count(int32_t n, int32_t keep_pct);
 
 /* Causal prefill attention for B sequences of s prompt tokens over the fp16
  * K, V straight from the QKV projection: out_i = sum_{pad[b]<=j<=i}
@@ -348,9 +357,11 @@ fg_status fg_prefill_attn(const fg_f16* qkv, int32_t B, int32_t s, int32_t H,
  * x_in, x_out: [bls*T][h1] fp16, sequence-major rows (may not alias).
  * cache->B must equal bls.  The k GPU batches are rows / cache sequences
  * [i*gbs, (i+1)*gbs).  workspace: device scratch of at least
- * fg_layer_workspace_bytes(w, phase, bls, T, p) bytes, 256-byte aligned. */
+ * fg_layer_workspace_bytes(w, phase, bls, T, cap, p) bytes, 256-byte
+ * aligned, cap the cache capacity (it sizes the scores of top-K decode
+ * attention, p.topk_pct in 1..99; otherwise it may be 0). */
 size_t fg_layer_workspace_bytes(const fg_layer* w, int32_t phase, int32_t bls,
-                                int32_t T, fg_policy p);
+                                int32_t T, int32_t cap, fg_policy p);
 fg_status fg_layer_step(const fg_layer* w, const fg_kv4* cache,
                         const fg_f16* x_in, fg_f16* x_out, int32_t phase,
                         int32_t T, int32_t pos, const int32_t* pad,

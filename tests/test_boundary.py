@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert fg.fg_version() >> 16 == 3
+    assert fg.fg_version() >> 16 == 4
     assert lib.fg_status_str(fg.FG_ERR_TIMEOUT) == b"device wait timed out"
 
 
@@ -68,11 +68,22 @@ def test_host_validation_rejects_without_launch(lib):
                                  None) == fg.FG_ERR_ALIGN               # pad misaligned
     for pct in (0, 101, -5):                                            # keep_pct outside [1, 100]
         assert lib.fg_decode_attn_topk_g4(P(0x5000), 384, ctypes.byref(kv), 7, None, pct, 1,
-                                          P(0x6000), None, None) == fg.FG_ERR_SHAPE
+                                          P(0x6000), None, P(0x8000), 1 << 20,
+                                          None) == fg.FG_ERR_SHAPE
     assert lib.fg_decode_attn_topk_g4(P(0x5000), 384, ctypes.byref(kv), 7, None, 10, 1,
-                                      P(0x6000), P(0x7001), None) == fg.FG_ERR_ALIGN   # sel_out
+                                      P(0x6000), P(0x7001), P(0x8000), 1 << 20,
+                                      None) == fg.FG_ERR_ALIGN                         # sel_out
     assert lib.fg_decode_attn_topk_g4(P(0x5000), 384, ctypes.byref(kv), 8, None, 10, 1,
-                                      P(0x6000), None, None) == fg.FG_ERR_SHAPE        # pos == cap
+                                      P(0x6000), None, P(0x8000), 1 << 20,
+                                      None) == fg.FG_ERR_SHAPE                         # pos == cap
+    assert lib.fg_decode_attn_topk_g4(P(0x5000), 384, ctypes.byref(kv), 7, None, 10, 1,
+                                      P(0x6000), None, P(0x8010), 1 << 20,
+                                      None) == fg.FG_ERR_ALIGN                         # workspace
+    need = lib.fg_decode_attn_topk_workspace_bytes(2, 2, 7)   # scores 2*2*8 fp32 + stats, 256-aligned
+    assert need == 512
+    assert lib.fg_decode_attn_topk_g4(P(0x5000), 384, ctypes.byref(kv), 7, None, 10, 1,
+                                      P(0x6000), None, P(0x8000), need - 1,
+                                      None) == fg.FG_ERR_WORKSPACE
     for n, pct, want in [(513, 10, 52), (1, 10, 1), (10, 10, 1), (11, 10, 2), (7, 100, 7),
                          (0, 10, 0), (5, 0, -1), (5, 101, -1), (-1, 10, -1)]:
         assert lib.fg_topk_count(n, pct) == want
@@ -111,7 +122,7 @@ def test_layer_step_validation(lib):
                    h1, H, h2, 1e-5)
     kv = fg.c_kv4(P(0x1000), P(0x2000), P(0x3000), P(0x4000), 4, H, 64, 16)
     pol = fg.c_policy(2, 3, 0)                                # bls 6 != cache B 4
-    need = lib.fg_layer_workspace_bytes(ctypes.byref(L), 0, 6, 8, pol)
+    need = lib.fg_layer_workspace_bytes(ctypes.byref(L), 0, 6, 8, 16, pol)
     assert need > 0
     st = lib.fg_layer_step(ctypes.byref(L), ctypes.byref(kv), P(0x5000), P(0x6000), 0, 8, 0,
                            None, pol, P(0x100000), need, None)
@@ -123,6 +134,13 @@ def test_layer_step_validation(lib):
     st = lib.fg_layer_step(ctypes.byref(L), ctypes.byref(kv), P(0x5000), P(0x6000), 1, 1, 3,
                            None, pol, P(0x100000), 16, None)
     assert st == fg.FG_ERR_WORKSPACE
+    dense = lib.fg_layer_workspace_bytes(ctypes.byref(L), 1, 4, 1, 16, pol)
+    topk = lib.fg_layer_workspace_bytes(ctypes.byref(L), 1, 4, 1, 16, fg.c_policy(2, 2, 0, 10))
+    assert topk == dense + lib.fg_decode_attn_topk_workspace_bytes(4, H, 15)
+    assert lib.fg_layer_workspace_bytes(ctypes.byref(L), 1, 4, 1, 16, fg.c_policy(2, 2, 0, 100)) == dense
+    st = lib.fg_layer_step(ctypes.byref(L), ctypes.byref(kv), P(0x5000), P(0x6000), 1, 1, 15,
+                           None, fg.c_policy(2, 2, 0, 10), P(0x100000), dense, None)
+    assert st == fg.FG_ERR_WORKSPACE                          # top-K needs its scores space
     for bad in (-1, 101):
         st = lib.fg_layer_step(ctypes.byref(L), ctypes.byref(kv), P(0x5000), P(0x6000), 1, 1, 3,
                                None, fg.c_policy(2, 2, 0, bad), P(0x100000), 1 << 30, None)

@@ -9,9 +9,9 @@ than those roundings may be kept by one side and not the other.  The tests
 therefore check (1) that the kernel's kept set is a valid top set against
 fp64 scores, and equal to the fp64 top set wherever the cut is clear of
 rounding; (2) the weighted sum against the oracle run on the kernel's own
-kept set; (3) exact identities: keeping every row is the dense kernel bit
-for bit, equal keys keep the lowest slots, the layer step's wiring equals
-the composition of the public calls."""
+kept set; (3) identities: keeping every row keeps every slot and gives the
+dense result, equal keys keep the lowest slots, the layer step's wiring
+equals the composition of the public calls bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -109,16 +109,21 @@ def test_topk_matches_oracle(B, H, d, L, pct, padded):
 
 @pytest.mark.parametrize("d,L,padded", [(64, 65, False), (128, 65, True), (128, 513, True),
                                         (64, 300, True), (128, 1100, False)])
-def test_keep_all_is_dense_bitwise(d, L, padded):
+def test_keep_all_matches_dense(d, L, padded):
+    """Keeping 100% of the rows keeps every slot and gives the dense result
+    (within the attention tolerance: the gather sums the same weights in
+    another order)."""
     B, H = 3, 2
-    _, g1 = _fill_cache(B, H, d, L + 1, L - 1, 77 + L)
+    oc, g1 = _fill_cache(B, H, d, L + 1, L - 1, 77 + L)
     _, g2 = _fill_cache(B, H, d, L + 1, L - 1, 77 + L)
     qkv = synth.normal_f16((B, 3 * H * d), 1.0, synth.generator(78)).to(DEV)
     pad = torch.tensor([0, 5, L - 1], dtype=torch.int32, device=DEV) if padded else None
     a, sel = fg.fg_decode_attn_topk_g4(qkv, g1, L - 1, 100, sel_out=True, pad=pad)
     b = fg.fg_decode_attn_g4(qkv, g2, L - 1, pad=pad)
     fg.fg_check()
-    assert torch.equal(a, b)
+    got, want = to_np(a).astype(np.float64), to_np(b).astype(np.float64)
+    assert np.all(np.abs(got - want) <= _attn_tol(want, oc, L))
+    assert rel_l2(got, want) < 2e-3
     s = to_np(sel)
     p0 = [0, 5, L - 1] if padded else [0, 0, 0]
     for i in range(B):
