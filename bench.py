@@ -503,6 +503,41 @@ def attn_case(B, H, d, L, iters, dev, seed=0, topk=0, kv="g4"):
     return sec, bytes_ / sec / 1e9
 
 
+def quant_case(iters, dev, seed=0):
+    """The group-wise 4-bit quantiser at HBM rate: (1) fg_quantize_g4 on one
+    OPT-30B fc1 matrix (28672 x 7168 fp16 -> codes + (min, scale)); (2) the
+    prefill's K/V store (the same quantiser on every prompt row's k and v,
+    into the cache) for 16 sequences of 512 tokens, 56 heads of 128, timed
+    by its trace class inside fg_prefill_attn.  Algorithmic bytes: 2 read +
+    0.625 written per element."""
+    from bit_group_quant_gb300 import fg
+    g = synth.generator(seed, dev)
+    N, K = 28672, 7168
+    x = synth.normal_f16((N, K), 0.02, g, dev)
+    q = fg.Q4.empty(N, K, dev)
+    sec = _time_launches(lambda: fg.fg_quantize_g4(x, out=q), iters, torch.cuda.current_stream())
+    fg.fg_check()
+    wq = {"elements": N * K, "ms": sec * 1e3, "gbs": 2.625 * N * K / sec / 1e9}
+    del x, q
+    B, S, H, d = 16, 512, 56, 128
+    qkv = synth.normal_f16((B * S, 3 * H * d), 1.0, g, dev)
+    cache = fg.KV4.empty(B, H, d, S, dev)
+    out = torch.empty((B * S, H * d), dtype=torch.float16, device=dev)
+    for _ in range(3):
+        fg.fg_prefill_attn(qkv, B, S, H, d, cache=cache, out=out)
+    torch.cuda.synchronize()
+    fg.fg_trace_begin(fg.FG_TRACE_OTHER)
+    for _ in range(iters):
+        fg.fg_prefill_attn(qkv, B, S, H, d, cache=cache, out=out)
+    torch.cuda.synchronize()
+    tr = fg.fg_trace_end()["other"]
+    fg.fg_check()
+    n = 2 * B * S * H * d
+    kv = {"elements": n, "ms": tr["ms"] / max(tr["launches"], 1),
+          "gbs": 2.625 * n / (tr["ms"] / max(tr["launches"], 1) / 1e3) / 1e9}
+    return wq, kv
+
+
 def prefill_case(B, s, H, d, iters, dev, seed=0):
     """One causal prefill-attention launch over fp16 Q/K/V of B sequences of s
     tokens; returns (seconds, causal TFLOP/s)."""
@@ -574,6 +609,12 @@ def run_micro(args):
         return {"micro": "prefill_attn", "B": args.B, "s": args.L, "H": args.H, "d": args.d,
                 "ms": sec * 1e3, "tflops_causal": tf, "frac_tensor": tf / peaks["bf16_tflops"],
                 "peak_source": kind + " bf16_tflops"}
+    if args.micro == "quant":
+        wq, kv = quant_case(args.iters, dev)
+        return {"micro": "quantize_g4", "weights_28672x7168": wq, "kv_store_B16_s512_H56_d128": kv,
+                "peak_hbm_gbs": peaks["hbm_gbs"], "frac_hbm": {"weights": wq["gbs"] / peaks["hbm_gbs"],
+                                                               "kv_store": kv["gbs"] / peaks["hbm_gbs"]},
+                "peak_source": kind + " hbm_gbs"}
     if args.micro == "attn":
         sec, gb = attn_case(args.B, args.H, args.d, args.L, args.iters, dev, topk=args.topk,
                             kv=args.kv)
@@ -668,7 +709,8 @@ def main(argv=None):
     ap.add_argument("--topk", type=int, default=0,
                     help="top-K sparse decode attention keeping this percent of the rows "
                          "(0: dense); the step, --micro attn and --micro decode")
-    ap.add_argument("--micro", choices=["gemm", "attn", "prefill", "sweep175b", "decode"], default=None,
+    ap.add_argument("--micro", choices=["gemm", "attn", "prefill", "sweep175b", "decode", "quant"],
+                    default=None,
                     help="time one kernel shape (or the OPT-175B layer sweep) instead")
     ap.add_argument("--M", type=int, default=4096)
     ap.add_argument("--residual", action="store_true",

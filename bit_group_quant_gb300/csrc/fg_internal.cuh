@@ -440,17 +440,24 @@ __device__ __forceinline__ uint32_t quantize8(const float (&v)[8], float& mn_out
     uint32_t packed = 0;
     if (scale != 0.0f) {
         const float inv = __frcp_rn(scale);
+        // Rounding to an integer by adding 1.5 * 2^23: for 0 <= t <= 15 the
+        // sum's unit in the last place is 1, so round-to-nearest-even of the
+        // sum is rint(t), and its low mantissa bits hold the integer.
+        // Clamping to [0, 15] first gives clamp(rint(t)) as the bounds are
+        // integers.
+        constexpr float kMagic = 12582912.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float num = __fsub_rn(v[i], mn);
-            // Fast quotient (within 2 ulp of the IEEE quotient); where it lies
+            // Fast quotient (within 3 ulp of the IEEE quotient); where it lies
             // that close to a rounding tie, take the IEEE division itself.
-            float t = __fmul_rn(num, inv);
-            const float frac = t - floorf(t);
-            if (fabsf(frac - 0.5f) < 1.0f / 65536.0f) t = __fdiv_rn(num, scale);
-            float r = rintf(t);
-            r = fminf(fmaxf(r, 0.0f), 15.0f);
-            packed |= static_cast<uint32_t>(r) << (4 * i);
+            float t = fminf(fmaxf(__fmul_rn(num, inv), 0.0f), 15.0f);
+            float m = __fadd_rn(t, kMagic);
+            if (fabsf(fabsf(__fsub_rn(t, __fsub_rn(m, kMagic))) - 0.5f) < 1.0f / 65536.0f) {
+                t = fminf(fmaxf(__fdiv_rn(num, scale), 0.0f), 15.0f);
+                m = __fadd_rn(t, kMagic);
+            }
+            packed |= (__float_as_uint(m) & 0xFu) << (4 * i);
         }
     }
     mn_out = mn;

@@ -90,7 +90,11 @@ __global__ void __launch_bounds__(256) dequant_g4_kernel(const uint32_t* __restr
 
 // KV-cache row store: token t of sequence b is qkv row (b*T + t); its k and v
 // parts (per head, groups of 64 along d) go to cache slot slot0 + t.
-// One group per 8 lanes, as in quantize_g4_kernel.
+// One group per 8 lanes, as in quantize_g4_kernel.  Groups are numbered
+// (k/v, sequence, head, token, group in the row) with the group in the row
+// fastest, then the token: consecutive groups go to consecutive cache rows of
+// one (sequence, head), so a warp's and its neighbours' codes and (min,
+// scale) stores are contiguous.
 __global__ void __launch_bounds__(256) kv_store_kernel(const __half* __restrict__ qkv, int64_t ld,
                                                        int32_t B, int32_t T, int32_t H,
                                                        int32_t d, int32_t cap, int32_t slot0,
@@ -102,24 +106,26 @@ __global__ void __launch_bounds__(256) kv_store_kernel(const __half* __restrict_
     const int sub = lane >> 3;
     const int lane8 = lane & 7;
     const int gpr = d / 64;                                   // groups per head row
-    const int64_t per_tok = static_cast<int64_t>(2) * H * gpr;  // k and v groups per token
-    const int64_t ngroups = static_cast<int64_t>(B) * T * per_tok;
+    const int64_t per_head = static_cast<int64_t>(T) * gpr;     // groups per (k/v, b, h)
+    const int64_t ngroups = static_cast<int64_t>(2) * B * H * per_head;
     const int64_t h1 = static_cast<int64_t>(H) * d;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     for (int64_t w = warp; w * 4 < ngroups; w += nwarps) {
         const int64_t g = w * 4 + sub;
         const bool valid = g < ngroups;
-        int64_t tok = 0, rem = 0;
+        int64_t tok = 0, t = 0, bh = 0;
         int is_v = 0, h = 0, gi = 0;
         float v[8];
         if (valid) {
-            tok = g / per_tok;
-            rem = g % per_tok;
-            is_v = static_cast<int>(rem / (static_cast<int64_t>(H) * gpr));
-            const int r2 = static_cast<int>(rem % (static_cast<int64_t>(H) * gpr));
-            h = r2 / gpr;
-            gi = r2 % gpr;
+            const int64_t head = g / per_head;           // (k/v, b, h)
+            const int64_t r2 = g % per_head;
+            t = r2 / gpr;
+            gi = static_cast<int>(r2 % gpr);
+            is_v = static_cast<int>(head / (static_cast<int64_t>(B) * H));
+            bh = head % (static_cast<int64_t>(B) * H);
+            h = static_cast<int>(bh % H);
+            tok = (bh / H) * T + t;
             const __half* src = qkv + tok * ld + (1 + is_v) * h1 + static_cast<int64_t>(h) * d +
                                 gi * 64 + lane8 * 8;
             unpack8(*reinterpret_cast<const uint4*>(src), v);
@@ -130,8 +136,7 @@ __global__ void __launch_bounds__(256) kv_store_kernel(const __half* __restrict_
         float mn, scale;
         const uint32_t packed = quantize8(v, mn, scale);
         if (valid) {
-            const int64_t b = tok / T, t = tok % T;
-            const int64_t row = (b * H + h) * cap + slot0 + t;
+            const int64_t row = bh * cap + slot0 + t;
             uint8_t* cdst = (is_v ? v_codes : k_codes) + row * (d / 2) + gi * 32;
             reinterpret_cast<uint32_t*>(cdst)[lane8] = packed;
             if (lane8 == 0) {
