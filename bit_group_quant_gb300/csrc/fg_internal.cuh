@@ -417,6 +417,33 @@ __device__ __forceinline__ bool total_less(float a, float b) {
 __device__ __forceinline__ float tmin(float a, float b) { return total_less(b, a) ? b : a; }
 __device__ __forceinline__ float tmax(float a, float b) { return total_less(a, b) ? b : a; }
 
+// The 4-bit code of num = x - min (>= 0): clamp(rint(num / scale), 0, 15)
+// with the IEEE quotient; inv = the IEEE reciprocal of scale.  The fast
+// quotient num * inv lies within 3 ulp of the IEEE one; where it lies that
+// close to a rounding tie, the IEEE division itself is taken.  Rounding to an
+// integer by adding 1.5 * 2^23: for 0 <= t <= 15 the sum's unit in the last
+// place is 1, so round-to-nearest-even of the sum is rint(t) and its low
+// mantissa bits hold the integer; clamping to [0, 15] first gives
+// clamp(rint(t)) as the bounds are integers.
+constexpr float kCodeMagic = 12582912.0f;
+// The fast code; *near_tie set when the fast quotient lies too close to a
+// rounding tie to decide it (then code4_exact decides).
+__device__ __forceinline__ uint32_t code4_fast(float num, float inv, bool* near_tie) {
+    const float t = fminf(fmaxf(__fmul_rn(num, inv), 0.0f), 15.0f);
+    const float m = __fadd_rn(t, kCodeMagic);
+    *near_tie = fabsf(fabsf(__fsub_rn(t, __fsub_rn(m, kCodeMagic))) - 0.5f) < 1.0f / 65536.0f;
+    return __float_as_uint(m) & 0xFu;
+}
+__device__ __forceinline__ uint32_t code4_exact(float num, float scale) {
+    const float t = fminf(fmaxf(__fdiv_rn(num, scale), 0.0f), 15.0f);
+    return __float_as_uint(__fadd_rn(t, kCodeMagic)) & 0xFu;
+}
+__device__ __forceinline__ uint32_t code4(float num, float inv, float scale) {
+    bool near_tie;
+    const uint32_t c = code4_fast(num, inv, &near_tie);
+    return near_tie ? code4_exact(num, scale) : c;
+}
+
 // Quantise one group of 64 values held by 8 consecutive lanes (8 values per
 // lane, lane8 = lane & 7 holds elements 8*lane8 .. 8*lane8+7).  Returns the
 // 8 codes packed into one word (element 8*lane8 in the lowest nibble) and
@@ -440,25 +467,8 @@ __device__ __forceinline__ uint32_t quantize8(const float (&v)[8], float& mn_out
     uint32_t packed = 0;
     if (scale != 0.0f) {
         const float inv = __frcp_rn(scale);
-        // Rounding to an integer by adding 1.5 * 2^23: for 0 <= t <= 15 the
-        // sum's unit in the last place is 1, so round-to-nearest-even of the
-        // sum is rint(t), and its low mantissa bits hold the integer.
-        // Clamping to [0, 15] first gives clamp(rint(t)) as the bounds are
-        // integers.
-        constexpr float kMagic = 12582912.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float num = __fsub_rn(v[i], mn);
-            // Fast quotient (within 3 ulp of the IEEE quotient); where it lies
-            // that close to a rounding tie, take the IEEE division itself.
-            float t = fminf(fmaxf(__fmul_rn(num, inv), 0.0f), 15.0f);
-            float m = __fadd_rn(t, kMagic);
-            if (fabsf(fabsf(__fsub_rn(t, __fsub_rn(m, kMagic))) - 0.5f) < 1.0f / 65536.0f) {
-                t = fminf(fmaxf(__fdiv_rn(num, scale), 0.0f), 15.0f);
-                m = __fadd_rn(t, kMagic);
-            }
-            packed |= (__float_as_uint(m) & 0xFu) << (4 * i);
-        }
+        for (int i = 0; i < 8; ++i) packed |= code4(__fsub_rn(v[i], mn), inv, scale) << (4 * i);
     }
     mn_out = mn;
     scale_out = scale;
