@@ -92,6 +92,50 @@ def test_opt30b_decode_layer_bls144_sampled():
         assert np.array_equal(to_np(meta[seqs, :, L]).reshape(oc_meta.shape), oc_meta)
 
 
+@pytest.mark.parametrize("L,kv", [(1024, "g4"), (512, "f16"), (1024, "f16")])
+def test_opt30b_decode_layer_bls144_context_and_cache_variants(L, kv):
+    """The benchmark's other OPT-30B configurations at full size: the decode
+    layer for the whole block of 144 sequences at context L + 1 (prompts of
+    1024 tokens, the pages' second padded length) and over the uncompressed
+    fp16 cache; 2 sampled sequences through the oracle (rel-L2 <= 5e-3).  The
+    fp16 cache's appended rows equal the layer's own k and v (recomputed
+    through the same kernels) bit for bit."""
+    wl = synth.OPT30B
+    g = synth.generator(31 + L, DEV)
+    w = synth.layer_weights(wl.h1, wl.h2, g, DEV)
+    w.update(synth.random_affine_params(wl.h1, wl.h2, g, DEV))
+    k, v = _kv_rows(wl.bls, wl.H, L, wl.d, g, DEV)
+    stack = LayerStack([quantize_layer(w, wl.h1, wl.H, wl.h2)], wl.gbs, wl.k, L + 1, DEV, kv=kv)
+    if kv == "f16":
+        c = fg.KV16.empty(wl.bls, wl.H, wl.d, L + 1, DEV)
+        c.k[:, :, :L] = k
+        c.v[:, :, :L] = v
+        stack.caches[0] = c
+    else:
+        stack.caches[0] = _gpu_cache(k, v, L + 1)
+    x = synth.normal_f16((wl.bls, wl.h1), 1.0, g, DEV)
+    y = stack.run(x, fg.FG_PHASE_DECODE, 1, L, fg.FG_ORDER_BLOCK)
+    fg.fg_check()
+    seqs = [0, 143]
+    ol = oracle_layer({n: to_np(t) for n, t in w.items()}, wl.h1, wl.H, wl.h2)
+    if kv == "f16":
+        oc = oracle.KVCache16(len(seqs), wl.H, wl.d, L + 1)
+        oc.k[:, :, :L] = to_np(k[seqs])
+        oc.v[:, :, :L] = to_np(v[seqs])
+    else:
+        oc = _oracle_cache(k, v, seqs, L + 1)
+    ref = layer_step(ol, to_np(x[seqs]), oc, DECODE, len(seqs), 1, pos=L)
+    assert rel_l2(to_np(y[seqs]), ref) <= 5e-3
+    if kv == "f16":
+        L0 = stack.layers[0]
+        a = fg.fg_layernorm(x[seqs], L0.ln1_g, L0.ln1_b)
+        qkv = fg.fg_dequant_gemm_g4(a, L0.qkv, bias=L0.b_qkv)
+        h1 = wl.h1
+        c = stack.caches[0]
+        assert torch.equal(c.k[seqs, :, L].reshape(len(seqs), h1), qkv[:, h1:2 * h1])
+        assert torch.equal(c.v[seqs, :, L].reshape(len(seqs), h1), qkv[:, 2 * h1:])
+
+
 @pytest.mark.parametrize("bls", synth.SWEEP_GEMM_BLS)
 @pytest.mark.parametrize("proj", ["qkv", "out", "fc1", "fc2"])
 def test_opt175b_dequant_gemm_sampled(bls, proj):
