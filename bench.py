@@ -398,7 +398,9 @@ def run_fg(args, ws, rank, local):
         "phase_ms_per_step": {"prefill": t_pre / args.steps * 1e3,
                               "decode": t_dec / args.steps * 1e3},
         "kernel_ms_per_step": {k: c["ms"] / args.steps for k, c in trace.items()},
-        "roofline": {"kernel": "gemm_tc_kernel<dequant> (prefill launches)", "bound": "tensor",
+        "roofline": {"kernel": "prefill projections: dequant_g4_kernel (weights to fp16, once per "
+                               "launch) + gemm_tc_kernel<fp16 weights>; time of both",
+                     "bound": "tensor",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak if achieved else None,
                      "peak_source": "%s bf16_tflops_sustained (fp16 dense rate = bf16)" % peak_kind,

@@ -50,7 +50,7 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 fg_status launch_quantize_g4(const __half* x, int64_t ngroups, uint8_t* codes, float* meta,
                              cudaStream_t st);
 fg_status launch_dequant_g4(const uint8_t* codes, const float* meta, int64_t ngroups,
-                            __half* x, cudaStream_t st);
+                            __half* x, cudaStream_t st, int trace_cls = FG_TRACE_OTHER);
 fg_status launch_kv_store(const __half* qkv, int64_t ld, int32_t B, int32_t T, int32_t H,
                           int32_t d, const fg_kv4* c, int32_t slot0, cudaStream_t st);
 fg_status launch_layernorm(const __half* x, int64_t rows, int64_t cols, int64_t x_ld,
@@ -89,11 +89,15 @@ struct GemmPlan {
     int feat_tiles;  // ceil(N / 128)
     int splits;      // K splits (grid.z); > 1 only when plan_rows fit one token tile
     int kc_per_split;  // K chunks (of 64) per split, a multiple of 4
-    size_t ws_bytes; // fp32 partial sums (and, for the TMEM kernel, its flags)
+    size_t ws_bytes; // fp32 partial sums (and, for the TMEM kernel, its flags), or the fp16 weights
+    size_t ws_min;   // what the launch cannot do without (the fp16 weights are optional)
     // the TMEM-operand kernel for one token tile of at most 160 rows
     // (gemm_dec.cu): clusters of dec_c CTAs share each activation stage;
     // dec_units = (feature tiles / dec_c) * (K / 256) units dealt out evenly
     // over dec_Q clusters
+    // prefill-sized blocks: the weights are dequantised once into fp16 at the
+    // start of the workspace and the fp16 pipeline multiplies them
+    int f16w;
     int dec;
     int dec_c, dec_Q, dec_nbox;
     long long dec_units;

@@ -50,6 +50,9 @@ constexpr int kDeqGroups = 4;        // groups of 2 warps; group g owns chunks i
 constexpr int kRasterGroup = 16;     // feature tiles per rasterisation group
 constexpr int kRotBlock = 4;         // feature tiles sharing one K-walk offset
 constexpr int kTileF = 128;          // output features per CTA (MMA M)
+// Planned rows from which the weights are dequantised once into fp16 for the
+// whole launch instead of once per 256-row token tile (the prefill).
+constexpr int64_t kF16WeightRows = 8192;
 constexpr int kChunk = 64;           // k per A/B stage: one 128-byte swizzle row of fp16
 constexpr int kCodeSpan = 4;         // K chunks per codes box (128 code bytes per row)
 constexpr uint32_t kABytes = kTileF * kChunk * 2;                // 16 KB
@@ -607,8 +610,10 @@ fg_status run_gemm(const void* X, const CUtensorMap& tmW, GemmParams& p, const f
     const double ybytes = kF32Out ? M * N * 4.0
                                   : (plan.splits > 1 ? plan.splits * M * N * 4.0
                                                      : M * N * 2.0 * (p.residual ? 2.0 : 1.0));
-    const int cls = !kDequant ? FG_TRACE_OTHER
-                              : (p.M > 256 ? FG_TRACE_GEMM_PREFILL : FG_TRACE_GEMM_DECODE);
+    // the LM head (fp32 logits) is traced with the small kernels; the
+    // projections by their size, whichever form the weights take
+    const int cls = kF32Out ? FG_TRACE_OTHER
+                            : (p.M > 256 ? FG_TRACE_GEMM_PREFILL : FG_TRACE_GEMM_DECODE);
     fg::TraceScope ts(cls, st, 2.0 * M * N * K, wbytes + M * K * 2.0 + ybytes);
     e = cudaLaunchKernelEx(&cfg, kern, tmX, tmW, p);
     if (e != cudaSuccess) return fg::cuda_error(e, "gemm launch");
@@ -686,6 +691,11 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int64_t plan_rows, bool dequ
         pl.kc_per_split = static_cast<int>(per);
     }
     pl.ws_bytes = pl.splits > 1 ? static_cast<size_t>(pl.splits) * M * N * sizeof(float) : 0;
+    pl.ws_min = pl.ws_bytes;
+    if (dequant && plan_rows >= kF16WeightRows) {   // splits == 1 here
+        pl.f16w = 1;
+        pl.ws_bytes = static_cast<size_t>(N) * K * sizeof(__half);
+    }
     return pl;
 }
 
@@ -695,10 +705,38 @@ fg_status launch_gemm_g4(const __half* X, int64_t M, const fg_q4* W, const __hal
     if (M == 0) return FG_OK;
     const int64_t N = W->rows, K = W->cols;
     const GemmPlan pl = plan_gemm(M, N, K, plan_rows);
-    if (pl.ws_bytes > 0 && (ws == nullptr || ws_bytes < pl.ws_bytes))
+    if (pl.ws_min > 0 && (ws == nullptr || ws_bytes < pl.ws_min))
         return set_error(FG_ERR_WORKSPACE, "dequant_gemm: workspace %zu < %zu bytes", ws_bytes,
-                         pl.ws_bytes);
+                         pl.ws_min);
     if (pl.dec) return launch_gemm_dec(X, M, W, bias, residual, act, Y, ws, ws_bytes, st, pl);
+    // prefill-sized blocks with room for the fp16 weights take the fp16
+    // pipeline; otherwise the fused dequantisation below
+    if (pl.f16w && ws != nullptr && ws_bytes >= pl.ws_bytes) {
+        // dequantise the weights once (exactly: fp16(fma(code, scale, min)),
+        // the values the fused path computes per tile), then the fp16 pipeline
+        __half* w16 = static_cast<__half*>(ws);
+        fg_status s = launch_dequant_g4(W->codes, W->meta, N * K / kGroup, w16, st,
+                                        FG_TRACE_GEMM_PREFILL);
+        if (s != FG_OK) return s;
+        CUtensorMap tmW;
+        s = make_tmap(&tmW, w16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, K, N, kChunk, kTileF,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+        if (s != FG_OK) return s;
+        GemmParams p{};
+        p.bias = bias;
+        p.residual = residual;
+        p.Y = Y;
+        p.M = static_cast<int>(M);
+        p.N = static_cast<int>(N);
+        p.K = static_cast<int>(K);
+        p.nt = pl.nt;
+        p.kchunks = static_cast<int>(K / kChunk);
+        p.kc_per_split = p.kchunks;
+        p.act = act;
+        p.status = device_status_ptr();
+        p.wait_ns = wait_limit_ns();
+        return run_gemm<false, false>(X, tmW, p, pl, st);
+    }
     // codes: one box = 128 rows x 128 bytes (4 K chunks), 128-byte swizzle
     CUtensorMap tmC;
     fg_status s = make_tmap(&tmC, W->codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N,

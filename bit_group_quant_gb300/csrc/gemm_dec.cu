@@ -671,6 +671,7 @@ bool plan_gemm_dec(int64_t M, int64_t N, int64_t K, int64_t plan_rows, GemmPlan&
     const size_t slots = static_cast<size_t>(pl.dec_Q) * c;
     pl.dec_part_bytes = (slots * pl.nt * kTileF * sizeof(float) + 255) & ~static_cast<size_t>(255);
     pl.ws_bytes = pl.dec_part_bytes + slots * 4 * sizeof(unsigned long long);
+    pl.ws_min = pl.ws_bytes;
     return true;
 }
 

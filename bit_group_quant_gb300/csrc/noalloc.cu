@@ -52,7 +52,9 @@ fg_status fg_dequant_gemm_g4_noalloc(const fg_f16* X, int64_t M, const fg_q4* W,
                                      const fg_f16* bias, const fg_f16* residual, int32_t act,
                                      fg_f16* Y, fg_stream stream) {
     if (W == nullptr) return fg::set_error(FG_ERR_NULL, "dequant_gemm_g4_noalloc: null fg_q4");
-    const size_t need = fg_dequant_gemm_workspace_bytes(M, W->rows, W->cols);
+    // the K-split partials it cannot do without (prefill-sized blocks, which
+    // would take fp16 weights from a caller workspace, use the fused path)
+    const size_t need = (M > 0 && W->rows > 0 && W->cols > 0) ? fg::plan_gemm(M, W->rows, W->cols).ws_min : 0;
     if (need > kNoAllocScratchBytes)
         return fg::set_error(FG_ERR_WORKSPACE,
                              "dequant_gemm_g4_noalloc: this shape needs %zu bytes of K-split "

@@ -238,10 +238,10 @@ fg_status launch_quantize_g4(const __half* x, int64_t ngroups, uint8_t* codes, f
 }
 
 fg_status launch_dequant_g4(const uint8_t* codes, const float* meta, int64_t ngroups,
-                            __half* x, cudaStream_t st) {
+                            __half* x, cudaStream_t st, int trace_cls) {
     if (ngroups == 0) return FG_OK;
     const int grid = grid_for(ngroups * 8, 256);
-    TraceScope ts(FG_TRACE_OTHER, st, 0.0, ngroups * (128.0 + 40.0));
+    TraceScope ts(trace_cls, st, 0.0, ngroups * (128.0 + 40.0));
     dequant_g4_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(codes),
                                             reinterpret_cast<const float2*>(meta), ngroups,
                                             reinterpret_cast<uint4*>(x));

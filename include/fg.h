@@ -182,16 +182,21 @@ fg_status fg_dequant_g4(const fg_q4* in, fg_f16* x, fg_stream stream);
  * Y: [M][N] fp16.  M >= 0 (M == 0 launches nothing); N % 16 == 0.
  * workspace: device scratch of at least
  * fg_dequant_gemm_workspace_bytes(M, N, K) bytes (NULL allowed when that is
- * 0), 256-byte aligned.
+ * 0), 256-byte aligned.  From M = 8192 rows that size is 2*N*K bytes: the
+ * weights are dequantised once into it and the fp16 tensor-core pipeline
+ * multiplies them (a prefill-sized block would otherwise dequantise every
+ * weight tile once per 256 rows); with less (or NULL) the same product is
+ * computed with the dequantisation fused per tile.
  * Each output is fp32-accumulated fp16(x) * fp16(w^) products with
  * w^ = fp16(fma(q, scale, min)) exactly as fg_dequant_g4 gives it.  The
  * result of a row never depends on the other rows; it depends on M only
- * through which of three regimes M falls in -- at most 144 rows with K a
- * multiple of 256 (the dequantised weights go to TMEM and K is split over
- * persistent CTA clusters, parts summed in a fixed order), at most 256 rows
- * (K split across CTAs, fixed-order sum), more than 256 rows (whole tiles) --
- * so launches in the same regime agree bit for bit.  The K split depends on
- * (N, K) and the device's SM count. */
+ * through which regime M falls in -- at most 144 rows with K a multiple of
+ * 256 (the dequantised weights go to TMEM and K is split over persistent
+ * CTA clusters, parts summed in a fixed order), at most 256 rows (K split
+ * across CTAs, fixed-order sum), more than 256 rows (whole tiles), 8192 rows
+ * or more with the full workspace (fp16 weights) -- so launches in the same
+ * regime agree bit for bit.  The K split depends on (N, K) and the device's
+ * SM count. */
 size_t fg_dequant_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 fg_status fg_dequant_gemm_g4(const fg_f16* X, int64_t M, const fg_q4* W,
                              const fg_f16* bias, const fg_f16* residual,
@@ -207,9 +212,9 @@ fg_status fg_dequant_gemm_g4(const fg_f16* X, int64_t M, const fg_q4* W,
  * passes X, W, bias, residual and Y); the K-split scratch comes from a
  * fixed 16 MiB device array inside the library (held on every GPU that
  * loads it until the process exits), so no workspace is passed and nothing
- * is allocated.  Shapes whose K-split scratch,
- * fg_dequant_gemm_workspace_bytes(M, N, K), exceeds 16 MiB are rejected
- * with FG_ERR_WORKSPACE before any launch.  The first call on a device
+ * is allocated; prefill-sized M takes the fused path (no fp16 weight
+ * copy).  Shapes whose K-split scratch exceeds 16 MiB are rejected with
+ * FG_ERR_WORKSPACE before any launch.  The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress) with that
  * device current; make that first call before any stream capture.  All
  * calls share the array and it keeps the last call's contents (no call
