@@ -24,6 +24,9 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 }
 
 // y = (x - mean) / sqrt(var + eps) * gamma + beta; mean, biased variance fp32.
+// One block per row; the row stays in registers as packed fp16 (4 registers
+// per 8 values, converted in each pass) so that enough rows are in flight
+// per SM to cover the load latency.
 __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const __half* __restrict__ x,
                                                                int64_t cols, int64_t x_ld,
                                                                const __half* __restrict__ g,
@@ -33,19 +36,20 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const __half* __r
     const int64_t row = blockIdx.x;
     const uint4* xr = reinterpret_cast<const uint4*>(x + row * x_ld);
     const int nvec = static_cast<int>(cols / 8);
-    float v[kLnMaxVec][8];
-    float s = 0.0f;
+    uint4 raw[kLnMaxVec];
 #pragma unroll
     for (int i = 0; i < kLnMaxVec; ++i) {
         const int c = threadIdx.x + i * kLnThreads;
-        if (c < nvec) {
-            const uint4 raw = xr[c];
-            const __half2* h = reinterpret_cast<const __half2*>(&raw);
+        raw[i] = c < nvec ? xr[c] : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kLnMaxVec; ++i) {
+        if (threadIdx.x + i * kLnThreads < nvec) {
+            const __half2* h = reinterpret_cast<const __half2*>(&raw[i]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float2 f = __half22float2(h[j]);
-                v[i][2 * j] = f.x;
-                v[i][2 * j + 1] = f.y;
                 s += f.x + f.y;
             }
         }
@@ -54,12 +58,15 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const __half* __r
     float q = 0.0f;
 #pragma unroll
     for (int i = 0; i < kLnMaxVec; ++i) {
-        const int c = threadIdx.x + i * kLnThreads;
-        if (c < nvec) {
+        if (threadIdx.x + i * kLnThreads < nvec) {
+            const __half2* h = reinterpret_cast<const __half2*>(&raw[i]);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float dv = __fsub_rn(v[i][j], mean);
-                q = __fadd_rn(q, __fmul_rn(dv, dv));
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = __half22float2(h[j]);
+                const float d0 = __fsub_rn(f.x, mean);
+                q = __fadd_rn(q, __fmul_rn(d0, d0));
+                const float d1 = __fsub_rn(f.y, mean);
+                q = __fadd_rn(q, __fmul_rn(d1, d1));
             }
         }
     }
@@ -73,18 +80,18 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const __half* __r
         const int c = threadIdx.x + i * kLnThreads;
         if (c < nvec) {
             const uint4 graw = gr[c], braw = br[c];
+            const __half2* xh = reinterpret_cast<const __half2*>(&raw[i]);
             const __half2* gh = reinterpret_cast<const __half2*>(&graw);
             const __half2* bh = reinterpret_cast<const __half2*>(&braw);
             uint4 out;
             __half2* oh = reinterpret_cast<__half2*>(&out);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
+                const float2 xf = __half22float2(xh[j]);
                 const float2 gf = __half22float2(gh[j]);
                 const float2 bf = __half22float2(bh[j]);
-                const float a0 = __fadd_rn(
-                    __fmul_rn(__fdiv_rn(__fsub_rn(v[i][2 * j], mean), denom), gf.x), bf.x);
-                const float a1 = __fadd_rn(
-                    __fmul_rn(__fdiv_rn(__fsub_rn(v[i][2 * j + 1], mean), denom), gf.y), bf.y);
+                const float a0 = __fadd_rn(__fmul_rn(__fdiv_rn(__fsub_rn(xf.x, mean), denom), gf.x), bf.x);
+                const float a1 = __fadd_rn(__fmul_rn(__fdiv_rn(__fsub_rn(xf.y, mean), denom), gf.y), bf.y);
                 oh[j] = __halves2half2(__float2half_rn(a0), __float2half_rn(a1));
             }
             yr[c] = out;
