@@ -1,5 +1,7 @@
 // attn.cu -- decode attention over the 4-bit KV cache (with the new token's
-// K/V append fused in) and causal prefill attention.
+// K/V append fused in), its top-K sparse form (a scores pass of the same
+// kernels, then one warp per (sequence, head) selecting the kept rows and
+// gathering their V), and causal prefill attention.
 //
 // Dataflow ("FlexGen 完全拆解", section on the inference dataflow): the
 // prefill computes Q, K, V for all prompt tokens; each decode step appends
