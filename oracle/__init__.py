@@ -11,7 +11,9 @@ what the C side reads), codes as ``np.uint8``, metadata as ``np.float32``.
 Parity status of each function (what pins it, in ``tests/test_oracle_*.py``):
   quantize_g4 / dequant_g4 .. pinned (nearest-level brute force, exact rational
                                worked group, reconstruction bound, constant and
-                               two-valued groups, nibble order fixture)
+                               two-valued groups, nibble order fixture; exact
+                               ties -> even codes, IEEE quotient vs reciprocal
+                               product, one fused multiply-add in dequant)
   linear_* .................. pinned (fp64 matmul within the fp32-accumulation
                                bound; permutation-matrix exactness)
   layernorm ................. pinned (fp64 closed form; zero-mean/unit-variance)

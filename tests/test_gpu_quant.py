@@ -104,3 +104,35 @@ def test_kv_append_bit_exact(B, H, d):
             assert np.array_equal(to_np(cache.v_meta[b, h, 5]), vm[0])
     # other slots untouched
     assert int(cache.k_codes[:, :, :5].sum()) == 0 and int(cache.v_meta[:, :, 6].abs().sum()) == 0
+
+
+def _golden_pins():
+    import json
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "rounding_pins.json")
+    with open(path, encoding="utf-8") as f:
+        return json.load(f)
+
+
+def test_quantize_dequant_hit_the_golden_rounding_pins():
+    """The hand-derived groups that separate rint from rounding half away,
+    the IEEE quotient from a reciprocal product, and one fused multiply-add
+    from a separate multiply and add: the kernels' codes and dequantised
+    values equal the fixture's expected values directly (no oracle)."""
+    pins = _golden_pins()
+    names = ["ties_half_even", "quotient_tie", "quotient_near_tie"]
+    x = np.array([pins[n]["x"] for n in names] + [pins["fma_dequant"]["x"]], np.float16)
+    q = fg.fg_quantize_g4(torch.from_numpy(x).to(DEV))
+    deq = fg.fg_dequant_g4(q)
+    # the fused GEMM dequantisation: X = I returns the dequantised weights
+    eye = torch.eye(64, dtype=torch.float16, device=DEV)
+    y = fg.fg_dequant_gemm_g4(eye, q)
+    torch.cuda.synchronize()
+    codes = to_np(q.codes)
+    got = np.stack([codes & 0xF, codes >> 4], -1).reshape(len(x), 64)
+    for i, n in enumerate(names):
+        assert np.array_equal(got[i], np.array(pins[n]["codes"])), n
+    p = pins["fma_dequant"]
+    assert got[3, p["index"]] == p["code"]
+    assert int(to_np(deq)[3, p["index"]].view(np.uint16)) == p["dequant_fp16_bits"]
+    assert int(to_np(y)[p["index"], 3].view(np.uint16)) == p["dequant_fp16_bits"]
