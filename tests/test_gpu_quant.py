@@ -121,7 +121,8 @@ def test_quantize_dequant_hit_the_golden_rounding_pins():
     values equal the fixture's expected values directly (no oracle)."""
     pins = _golden_pins()
     names = ["ties_half_even", "quotient_tie", "quotient_near_tie"]
-    x = np.array([pins[n]["x"] for n in names] + [pins["fma_dequant"]["x"]], np.float16)
+    x = np.zeros((16, 64), np.float16)      # the GEMM takes N in multiples of 16
+    x[:4] = np.array([pins[n]["x"] for n in names] + [pins["fma_dequant"]["x"]], np.float16)
     q = fg.fg_quantize_g4(torch.from_numpy(x).to(DEV))
     deq = fg.fg_dequant_g4(q)
     # the fused GEMM dequantisation: X = I returns the dequantised weights
@@ -129,7 +130,7 @@ def test_quantize_dequant_hit_the_golden_rounding_pins():
     y = fg.fg_dequant_gemm_g4(eye, q)
     torch.cuda.synchronize()
     codes = to_np(q.codes)
-    got = np.stack([codes & 0xF, codes >> 4], -1).reshape(len(x), 64)
+    got = np.stack([codes & 0xF, codes >> 4], -1).reshape(16, 64)
     for i, n in enumerate(names):
         assert np.array_equal(got[i], np.array(pins[n]["codes"])), n
     p = pins["fma_dequant"]
