@@ -14,7 +14,13 @@ namespace {
 
 thread_local char g_err[512];
 
-__device__ int g_dev_status;   // FG device status word, one per device
+// FG device status word, one per device: [0] the first error code a kernel
+// reported (0: none), [1] how many times fg_check has cleared an error.  The
+// second word lets kernels that tag cross-CTA flags with a per-launch value
+// (the decode GEMM's fixup) change that value after a failed launch, so a
+// replay of the same launch (a CUDA graph) never accepts a flag the failed
+// launch left behind.
+__device__ int g_dev_status[2];
 
 constexpr int kMaxDevices = 64;
 int* g_status_ptr[kMaxDevices];
@@ -417,8 +423,10 @@ fg_status fg_check(fg_stream stream) {
     e = cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return fg::cuda_error(e, "fg_check read");
     if (v != 0) {
-        const int zero = 0;
-        cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        int gen = 0;
+        cudaMemcpy(&gen, p + 1, sizeof(int), cudaMemcpyDeviceToHost);
+        const int words[2] = {0, gen + 1};
+        cudaMemcpy(p, words, sizeof(words), cudaMemcpyHostToDevice);
         return fg::set_error(FG_ERR_TIMEOUT, "a bounded device wait expired (code %d)", v);
     }
     return FG_OK;

@@ -230,6 +230,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
         report(p.status, fg::kDevTimeout);
     };
+    // The flags' tag: the launch's own value, changed by the count of errors
+    // fg_check has cleared, so flags left set by a launch that timed out can
+    // never match a later replay of it.
+    const unsigned long long epoch =
+        p.epoch ^ (p.status != nullptr
+                       ? static_cast<unsigned long long>(
+                             static_cast<uint32_t>(reinterpret_cast<volatile int*>(p.status)[1]) & 0xFFFFu)
+                             << 32
+                       : 0ull);
 
     // Later parts of the tile whose first part ends this cluster's range:
     // computed by clusters q + 1, q + 2, ... (in k order), each published by
@@ -243,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const unsigned long long* f = p.flags + (r * c + static_cast<int>(crank)) * 4 + qq;
             const uint64_t t0 = globaltimer();
             bool got = true;
-            while (ld_acquire_u64(f) != p.epoch) {
+            while (ld_acquire_u64(f) != epoch) {
                 if (*abort_flag || globaltimer() - t0 > lim) {
                     got = false;
                     break;
@@ -565,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) st_release_u64(p.flags + slot * 4 + qq, p.epoch);
+                if (lane == 0) st_release_u64(p.flags + slot * 4 + qq, epoch);
             } else {
                 // The tile's first part (or the whole tile); in the last
                 // segment shared with the dequantisers (chunks 0, 4, 8, ...).

@@ -52,8 +52,11 @@ fg_status fg_dequant_gemm_g4_noalloc(const fg_f16* X, int64_t M, const fg_q4* W,
                                      const fg_f16* bias, const fg_f16* residual, int32_t act,
                                      fg_f16* Y, fg_stream stream) {
     if (W == nullptr) return fg::set_error(FG_ERR_NULL, "dequant_gemm_g4_noalloc: null fg_q4");
-    // the K-split partials it cannot do without (prefill-sized blocks, which
-    // would take fp16 weights from a caller workspace, use the fused path)
+    // Only the scratch a shape cannot do without: the K-split partial sums
+    // (and the decode kernel's fixup flags).  Prefill-sized blocks, which
+    // would put an fp16 copy of the weights into a large enough workspace,
+    // are offered exactly `need` bytes, so they always take the fused path
+    // and the array never holds a weight copy.
     const size_t need = (M > 0 && W->rows > 0 && W->cols > 0) ? fg::plan_gemm(M, W->rows, W->cols).ws_min : 0;
     if (need > kNoAllocScratchBytes)
         return fg::set_error(FG_ERR_WORKSPACE,
@@ -64,10 +67,13 @@ fg_status fg_dequant_gemm_g4_noalloc(const fg_f16* X, int64_t M, const fg_q4* W,
     void* scratch = nullptr;
     fg_status s = scratch_address(&scratch);
     if (s != FG_OK) return s;
-    // Nothing in the scratch has to start at zero: every partial sum the
-    // reduction reads is written earlier in the same call.
-    return fg_dequant_gemm_g4(X, M, W, bias, residual, act, Y, scratch, kNoAllocScratchBytes,
-                              stream);
+    // Nothing in the scratch has to start at zero.  Every partial sum read is
+    // written earlier in the same call.  The decode kernel's fixup flags (after
+    // its partial sums) hold a per-launch tag, set once a part is written and
+    // cleared once it is consumed; the tag also changes after fg_check reports
+    // a timeout, so flags a failed call left set never match a later call.
+    return fg_dequant_gemm_g4(X, M, W, bias, residual, act, Y, need > 0 ? scratch : nullptr,
+                              need, stream);
 }
 
 }  // extern "C"

@@ -196,7 +196,14 @@ fg_status fg_dequant_g4(const fg_q4* in, fg_f16* x, fg_stream stream);
  * across CTAs, fixed-order sum), more than 256 rows (whole tiles), 8192 rows
  * or more with the full workspace (fp16 weights) -- so launches in the same
  * regime agree bit for bit.  The K split depends on (N, K) and the device's
- * SM count. */
+ * SM count.
+ * In the first regime (at most 144 rows) the tiles split over clusters are
+ * finished by the cluster holding their first part, which waits for the
+ * later parts behind flags in the workspace; the grid is sized so that
+ * every cluster can be resident at once.  If another context on the same
+ * GPU keeps some clusters from being scheduled, those waits expire after
+ * the bounded-wait limit and the call reports FG_ERR_TIMEOUT through
+ * fg_check, with Y unspecified (never a hang). */
 size_t fg_dequant_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 fg_status fg_dequant_gemm_g4(const fg_f16* X, int64_t M, const fg_q4* W,
                              const fg_f16* bias, const fg_f16* residual,
@@ -212,14 +219,17 @@ fg_status fg_dequant_gemm_g4(const fg_f16* X, int64_t M, const fg_q4* W,
  * passes X, W, bias, residual and Y); the K-split scratch comes from a
  * fixed 16 MiB device array inside the library (held on every GPU that
  * loads it until the process exits), so no workspace is passed and nothing
- * is allocated; prefill-sized M takes the fused path (no fp16 weight
- * copy).  Shapes whose K-split scratch exceeds 16 MiB are rejected with
- * FG_ERR_WORKSPACE before any launch.  The first call on a device
- * looks up the array's device address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture.  All
- * calls share the array and it keeps the last call's contents (no call
- * relies on them: every partial sum read is written earlier in the same
- * call); calls that overlap on the GPU -- on different streams of one
+ * is allocated.  The call offers the GEMM only the scratch the shape cannot
+ * do without, so M >= 8192 always takes the fused path (the weights are
+ * never copied into the array as fp16).  Shapes whose K-split scratch
+ * exceeds 16 MiB are rejected with FG_ERR_WORKSPACE before any launch.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the array and it keeps the
+ * last call's contents.  No call relies on them: every partial sum read is
+ * written earlier in the same call, and the decode kernel's fixup flags
+ * carry a per-launch tag that also changes after fg_check reports a
+ * timeout.  Calls that overlap on the GPU -- on different streams of one
  * device -- race on it and must be serialised by the caller. */
 fg_status fg_dequant_gemm_g4_noalloc(const fg_f16* X, int64_t M, const fg_q4* W,
                                      const fg_f16* bias, const fg_f16* residual,

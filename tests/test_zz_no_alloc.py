@@ -43,7 +43,7 @@ def _noalloc_c(x, q, b, r, act, y):
 
 def _check_against_existing(x, q, b, r, act):
     M, N = x.shape[0], q.rows
-    assert fg.fg_dequant_gemm_workspace_bytes(M, N, q.cols) > 0   # the K-split scratch path
+    assert fg.fg_dequant_gemm_workspace_bytes(M, N, q.cols) > 0   # a path that needs scratch
     y_new = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
     assert _noalloc_c(x, q, b, r, act, y_new) == fg.FG_OK, fg.load().fg_last_error()
     y_old = fg.fg_dequant_gemm_g4(x, q, bias=b, residual=r, act=act)
@@ -53,7 +53,9 @@ def _check_against_existing(x, q, b, r, act):
     bound = gemm_bound(to_np(x), codes, meta) + ulp16(want)
     assert np.all(np.abs(got - want) <= bound)
     assert rel_l2(got, want) < 2e-3
-    # the same kernel and plan run on both sides, so the results agree exactly
+    # the same kernel and plan run on both sides (at M >= 8192 the fused path
+    # against the weights dequantised once: the same values in the same K
+    # order), so the results agree exactly
     assert torch.equal(y_new, y_old)
 
 
@@ -63,6 +65,24 @@ def test_noalloc_matches_existing_entry_point_twice():
     # second call right after, other shape and inputs: the scratch keeps the
     # first call's partials, and none of them may leak into this result
     _check_against_existing(*_inputs(144, 512, 4096, 2), act=0)
+
+
+def test_noalloc_split_k_across_ctas_twice():
+    # 161..256 rows: one token tile with K split across CTAs, fp32 partials in
+    # the built-in array, then summed in a fixed order by a second kernel
+    assert fg.fg_dequant_gemm_workspace_bytes(200, 512, 4096) <= fg.NOALLOC_SCRATCH_BYTES
+    _check_against_existing(*_inputs(200, 512, 4096, 3), act=1)
+    _check_against_existing(*_inputs(232, 256, 2048, 4), act=0)
+
+
+def test_noalloc_prefill_sized_block_uses_no_weight_copy():
+    # M >= 8192: the allocating entry point dequantises the weights once into
+    # its workspace; this call is offered no scratch for that and takes the
+    # fused path, with the same result
+    M, N, K = 8192 + 48, 256, 512
+    assert fg.fg_dequant_gemm_workspace_bytes(M, N, K) == N * K * 2
+    _check_against_existing(*_inputs(M, N, K, 5), act=0)
+    _check_against_existing(*_inputs(M, N, K, 6), act=1)
 
 
 def test_noalloc_rejects_scratch_beyond_its_maximum():
