@@ -13,8 +13,11 @@ bls 144, s 512, n 32, weights and KV cache 4-bit g64, all resident in HBM.
 ranks over the max-over-ranks time.  Inputs (18.5 GB of weights, 33.7 GB of
 KV cache) are far larger than L2, so no flush is needed between steps.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-Under torchrun each rank runs an independent replica on its own GPU.
+python bench.py [--steps K] [--warmup W] [--impl reference]
+The product runs on one GPU: under torchrun with more than one rank it
+prints an "unavailable" line and touches no GPU (the GEMM kernels' cluster
+multicast loads stay in single-GPU runs; sequences are independent, so N
+GPUs are N separate jobs).
 """
 from __future__ import annotations
 
@@ -216,7 +219,20 @@ def oracle_sample(wl, nseq: int, seed: int = 0, frac: int = 16):
 # the GPU arm
 # --------------------------------------------------------------------------
 
+# Why a run with more than one process is refused: the dequant-GEMM kernels
+# share activation tiles across a thread-block cluster with multicast bulk
+# tensor loads, which are kept to runs that use a single GPU.  Sequences are
+# independent, so N GPUs are N separate single-GPU jobs.
+MULTI_GPU_REFUSAL = ("one GPU per run: the dequant-GEMM kernels use cluster-multicast "
+                     "bulk tensor loads, which stay in single-GPU runs; run N independent "
+                     "single-GPU jobs instead")
+
+
 def run_fg(args, ws, rank, local):
+    if ws > 1:
+        # no GPU is touched; rank 0 alone says why
+        return ({"metric": METRIC, "unit": UNIT, "n_gpus": ws, "unavailable": MULTI_GPU_REFUSAL}
+                if rank == 0 else None)
     from bit_group_quant_gb300 import fg
     from bit_group_quant_gb300.model import random_model
 
@@ -726,6 +742,11 @@ def main(argv=None):
     ap.add_argument("--iters", type=int, default=10)
     args = ap.parse_args(argv)
     ws, rank, local = dist_env()
+    if ws > 1 and args.impl != "reference":
+        line = run_fg(args, ws, rank, local)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
     if args.micro:
         print(json.dumps(run_micro(args)), flush=True)
         return

@@ -49,3 +49,15 @@ def test_single_process_aggregation_is_identity():
     import bench
     v, t = bench.aggregate(100.0, 4.0)
     assert v == 25.0 and t == 4.0
+
+
+def test_product_arm_refuses_more_than_one_rank_without_touching_a_gpu():
+    """The product runs on one GPU (its GEMMs use cluster-multicast loads,
+    kept to single-GPU runs): with WORLD_SIZE > 1, rank 0 reports the line
+    as unavailable and the other ranks print nothing."""
+    import argparse
+    import bench
+    args = argparse.Namespace()
+    line = bench.run_fg(args, 2, 0, 0)
+    assert line["unavailable"] == bench.MULTI_GPU_REFUSAL and line["n_gpus"] == 2
+    assert bench.run_fg(args, 2, 1, 1) is None
