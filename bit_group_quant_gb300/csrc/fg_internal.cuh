@@ -124,6 +124,11 @@ fg_status launch_gemm_dec(const __half* X, int64_t M, const fg_q4* W, const __ha
 fg_status make_tmap(CUtensorMap* tm, const void* ptr, CUtensorMapDataType dt, int esize,
                     uint64_t cols, uint64_t rows, uint32_t bx, uint32_t by,
                     CUtensorMapSwizzle swz);
+// gemm_pf.cu: Y = act(X W16^T + bias) + residual with fp16 weights W16 [N][K]
+// on CTA pairs (the prefill regime, weights dequantised once beforehand).
+fg_status launch_gemm_pf(const __half* X, int64_t M, const __half* W16, int64_t N, int64_t K,
+                         const __half* bias, const __half* residual, int act, __half* Y,
+                         cudaStream_t st);
 fg_status launch_gemm_f16_f32out(const __half* X, int64_t M, const __half* W, int64_t N,
                                  int64_t K, float* Y, cudaStream_t st);
 
@@ -359,6 +364,87 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---- CTA pairs (cta_group::2): one MMA over two SMs of a 2-CTA cluster.
+// M = 256 rows, the even CTA's 128 rows and the odd CTA's 128 rows of A at
+// the same shared-memory offset; N split in halves, columns 0..N/2-1 from the
+// even CTA's B and N/2..N-1 from the odd CTA's; each CTA's TMEM receives its
+// own 128 rows of D.  Issued by the even CTA only.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(ncols)
+                 : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T over the pair, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on the mbarrier at the same offset in every CTA of `mask` when
+// all pair MMAs previously issued by this thread have completed.
+__device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier that may sit in the peer CTA of the pair (bar: shared::cluster
+// address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tm, int x, int y,
+                                                 uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(tm), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+// Arrive (release, cluster scope) on an mbarrier of another CTA of the
+// cluster (bar: shared::cluster address from mapa_shared).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait (acquire, cluster scope) for a barrier that other CTAs of the
+// cluster arrive on; same contract as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort, uint64_t limit_ns) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((i & 31u) == 0) {
+            if (abort != nullptr && *abort) return false;
+            if (globaltimer() - t0 > limit_ns) return false;
+        }
+    }
 }
 
 // ---- flags between CTAs of one grid (global memory, gpu scope)

@@ -713,29 +713,13 @@ fg_status launch_gemm_g4(const __half* X, int64_t M, const fg_q4* W, const __hal
     // pipeline; otherwise the fused dequantisation below
     if (pl.f16w && ws != nullptr && ws_bytes >= pl.ws_bytes) {
         // dequantise the weights once (exactly: fp16(fma(code, scale, min)),
-        // the values the fused path computes per tile), then the fp16 pipeline
+        // the values the fused path computes per tile), then the fp16 GEMM on
+        // CTA pairs (gemm_pf.cu)
         __half* w16 = static_cast<__half*>(ws);
         fg_status s = launch_dequant_g4(W->codes, W->meta, N * K / kGroup, w16, st,
                                         FG_TRACE_GEMM_PREFILL);
         if (s != FG_OK) return s;
-        CUtensorMap tmW;
-        s = make_tmap(&tmW, w16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, K, N, kChunk, kTileF,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-        if (s != FG_OK) return s;
-        GemmParams p{};
-        p.bias = bias;
-        p.residual = residual;
-        p.Y = Y;
-        p.M = static_cast<int>(M);
-        p.N = static_cast<int>(N);
-        p.K = static_cast<int>(K);
-        p.nt = pl.nt;
-        p.kchunks = static_cast<int>(K / kChunk);
-        p.kc_per_split = p.kchunks;
-        p.act = act;
-        p.status = device_status_ptr();
-        p.wait_ns = wait_limit_ns();
-        return run_gemm<false, false>(X, tmW, p, pl, st);
+        return launch_gemm_pf(X, M, w16, N, K, bias, residual, act, Y, st);
     }
     // codes: one box = 128 rows x 128 bytes (4 K chunks), 128-byte swizzle
     CUtensorMap tmC;

@@ -32,8 +32,10 @@ def short_waits():
 
 
 # M 16 with K a multiple of 256: the TMEM-operand kernel; M 200: one token
-# tile with K split across CTAs; M 300: whole tiles
-@pytest.mark.parametrize("M,N,K", [(16, 512, 1024), (200, 384, 512), (300, 256, 640)])
+# tile with K split across CTAs; M 300: whole tiles; M 8192: the weights
+# dequantised once, then the CTA-pair GEMM
+@pytest.mark.parametrize("M,N,K", [(16, 512, 1024), (200, 384, 512), (300, 256, 640),
+                                   (8192, 384, 512)])
 def test_dropped_arrive_reports_timeout_and_context_survives(short_waits, M, N, K):
     g = synth.generator(M + N + K, DEV)
     x = synth.normal_f16((M, K), 1.0, g, DEV)

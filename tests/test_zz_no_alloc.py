@@ -41,7 +41,7 @@ def _noalloc_c(x, q, b, r, act, y):
     return st
 
 
-def _check_against_existing(x, q, b, r, act):
+def _check_against_existing(x, q, b, r, act, exact=True):
     M, N = x.shape[0], q.rows
     assert fg.fg_dequant_gemm_workspace_bytes(M, N, q.cols) > 0   # a path that needs scratch
     y_new = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
@@ -53,10 +53,11 @@ def _check_against_existing(x, q, b, r, act):
     bound = gemm_bound(to_np(x), codes, meta) + ulp16(want)
     assert np.all(np.abs(got - want) <= bound)
     assert rel_l2(got, want) < 2e-3
-    # the same kernel and plan run on both sides (at M >= 8192 the fused path
-    # against the weights dequantised once: the same values in the same K
-    # order), so the results agree exactly
-    assert torch.equal(y_new, y_old)
+    # the same kernel and plan run on both sides, so the results agree
+    # exactly (at M >= 8192 the allocating call multiplies weights dequantised
+    # once into its workspace, in another summation order: the bound above)
+    if exact:
+        assert torch.equal(y_new, y_old)
 
 
 def test_noalloc_matches_existing_entry_point_twice():
@@ -78,11 +79,11 @@ def test_noalloc_split_k_across_ctas_twice():
 def test_noalloc_prefill_sized_block_uses_no_weight_copy():
     # M >= 8192: the allocating entry point dequantises the weights once into
     # its workspace; this call is offered no scratch for that and takes the
-    # fused path, with the same result
+    # fused path, with the same result up to the fp32 summation order
     M, N, K = 8192 + 48, 256, 512
     assert fg.fg_dequant_gemm_workspace_bytes(M, N, K) == N * K * 2
-    _check_against_existing(*_inputs(M, N, K, 5), act=0)
-    _check_against_existing(*_inputs(M, N, K, 6), act=1)
+    _check_against_existing(*_inputs(M, N, K, 5), act=0, exact=False)
+    _check_against_existing(*_inputs(M, N, K, 6), act=1, exact=False)
 
 
 def test_noalloc_rejects_scratch_beyond_its_maximum():
