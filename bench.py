@@ -415,12 +415,12 @@ def run_fg(args, ws, rank, local):
                               "decode": t_dec / args.steps * 1e3},
         "kernel_ms_per_step": {k: c["ms"] / args.steps for k, c in trace.items()},
         "roofline": {"kernel": "prefill projections: dequant_g4_kernel (weights to fp16, once per "
-                               "launch) + gemm_tc_kernel<fp16 weights>; time of both",
+                               "launch) + gemm_pf_kernel (CTA-pair tcgen05 GEMM); time of both",
                      "bound": "tensor",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak if achieved else None,
                      "peak_source": "%s bf16_tflops_sustained (fp16 dense rate = bf16)" % peak_kind,
-                     "traffic": committed_traffic("gemm.cu", wl.name),
+                     "traffic": committed_traffic("gemm_pf.cu", wl.name),
                      "launches": gp["launches"],
                      "avg_launch_ms": gp["ms"] / max(gp["launches"], 1)},
         "decode_roofline": {
