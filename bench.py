@@ -238,6 +238,8 @@ def run_fg(args, ws, rank, local):
 
     wl = synth.WORKLOADS[args.workload]
     D = wl.decode_steps
+    if wl.vocab == 0:
+        return run_layer_workload(args, wl, local)
 
     cpu_base = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -672,6 +674,115 @@ def run_micro(args):
     return {"sweep": "opt-175b layer: h1 12288, 96 heads of 128, h2 49152",
             "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tflops")}, "peak_source": kind,
             "dequant_gemm": gemm, "decode_attn_bls144": attn}
+
+
+def run_layer_workload(args, wl, local):
+    """The single-decoder-layer workload (no embedding, no LM head): a block
+    of bls sequences fed N(0, 1) hidden states, prefill of s prompt tokens,
+    then decode_steps teacher-forced decode steps, each fed a new hidden
+    state per sequence.  value = bls * decode_steps / decode time."""
+    import oracle
+    from bit_group_quant_gb300 import fg
+    from bit_group_quant_gb300.model import LayerStack, quantize_layer
+    from oracle.model import DECODE, PREFILL, layer_step
+    from oracle.model import quantize_layer as oracle_layer
+
+    D = wl.decode_steps
+    torch.cuda.set_device(local)
+    dev = "cuda:%d" % local
+    stream = torch.cuda.current_stream()
+    gw = synth.generator(0, dev)
+    w = synth.layer_weights(wl.h1, wl.h2, gw, dev)
+    stack = LayerStack([quantize_layer(w, wl.h1, wl.H, wl.h2)], wl.gbs, wl.k, wl.s + D, dev)
+    g = synth.generator(1000, dev)
+    x_pre = synth.normal_f16((wl.bls * wl.s, wl.h1), 1.0, g, dev)
+    x_dec = synth.normal_f16((D, wl.bls, wl.h1), 1.0, g, dev)
+    y_pre = torch.empty_like(x_pre)
+    y_dec = torch.empty_like(x_dec)
+    order = fg.FG_ORDER_BLOCK
+
+    def step(evs=None, xp=x_pre, xd=x_dec):
+        if evs:
+            evs[0].record(stream)
+        stack.run(xp, fg.FG_PHASE_PREFILL, wl.s, 0, order, out=y_pre)
+        if evs:
+            evs[1].record(stream)
+        for t in range(1, D + 1):
+            stack.run(xd[t - 1], fg.FG_PHASE_DECODE, 1, wl.s + t - 1, order, out=y_dec[t - 1])
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    fg.fg_check()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    torch.cuda.synchronize()
+    clocks.start()
+    fg.fg_trace_begin(0)
+    for k in range(args.steps):
+        step(evs[k])
+    torch.cuda.synchronize()
+    trace = fg.fg_trace_end()
+    clk = clocks.stop()
+    fg.fg_check()
+    t_pre = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+    t_dec = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+    value = wl.bls * D * args.steps / t_dec
+    # end to end: hidden states in from pinned host memory, the last decode
+    # step's output back, every step
+    e2e = None
+    if not args.no_e2e:
+        h_pre = x_pre.cpu().pin_memory()
+        h_dec = x_dec.cpu().pin_memory()
+        h_out = torch.empty_like(y_dec[-1], device="cpu").pin_memory()
+        d_pre, d_dec = torch.empty_like(x_pre), torch.empty_like(x_dec)
+        tot_dec = 0.0
+        for k in range(args.steps):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+            ev[0].record(stream)
+            d_pre.copy_(h_pre, non_blocking=True)
+            d_dec.copy_(h_dec, non_blocking=True)
+            ev[1].record(stream)
+            step(ev[2:5], xp=d_pre, xd=d_dec)
+            h_out.copy_(y_dec[-1], non_blocking=True)
+            ev[5].record(stream)
+            torch.cuda.synchronize()
+            # the copies in (prompt and decode inputs), the decode phase, the copy out
+            tot_dec += (ev[0].elapsed_time(ev[1]) + ev[3].elapsed_time(ev[5])) / 1e3
+        e2e = {"value": wl.bls * D * args.steps / tot_dec, "unit": UNIT,
+               "h2d_bytes_per_step": int(h_pre.numel() * 2 + h_dec.numel() * 2),
+               "d2h_bytes_per_step": int(h_out.numel() * 2),
+               "note": "decode phase plus the read-back of the last decode step's hidden states; "
+                       "the hidden-state inputs are copied in from pinned memory every step"}
+    cpu_base = None
+    if not args.no_cpu_baseline:
+        # the oracle on the whole workload (it is small): prefill + D decode steps
+        ol = oracle_layer({n: t.cpu().numpy() for n, t in w.items()}, wl.h1, wl.H, wl.h2)
+        cache = oracle.KVCache(wl.bls, wl.H, wl.d, wl.s + D)
+        xp, xd = x_pre.cpu().numpy(), x_dec.cpu().numpy()
+        t0 = time.perf_counter()
+        layer_step(ol, xp, cache, PREFILL, wl.bls, wl.s)
+        t1 = time.perf_counter()
+        for t in range(1, D + 1):
+            layer_step(ol, xd[t - 1], cache, DECODE, wl.bls, 1, pos=wl.s + t - 1)
+        t2 = time.perf_counter()
+        cpu_base = {"value": wl.bls * D / (t2 - t1), "unit": UNIT, "cores": oracle.num_threads(),
+                    "kind": "oracle",
+                    "sample": "the whole workload (prefill %.2f s, %d decode steps %.2f s)"
+                              % (t1 - t0, D, t2 - t1)}
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": (t_pre + t_dec) / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
+            "data": "synthetic",
+            "config": {"workload": "%s: one decoder layer, h1 %d, %d heads, h2 %d; gbs %d x k %d, "
+                                   "s %d, %d teacher-forced decode steps; weights and KV 4-bit g64"
+                                   % (wl.name, wl.h1, wl.H, wl.h2, wl.gbs, wl.k, wl.s, D),
+                       "l2": "inputs smaller than L2 (a latency-bound workload; no flush)"},
+            "phase_ms_per_step": {"prefill": t_pre / args.steps * 1e3,
+                                  "decode": t_dec / args.steps * 1e3},
+            "gpu_launches": int(sum(c["launches"] for c in trace.values())),
+            "cpu_baseline": cpu_base, "e2e": e2e, "clocks": clk}
 
 
 def run_reference(args, ws, rank):
