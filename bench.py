@@ -265,24 +265,36 @@ def run_fg(args, ws, rank, local):
                   for _ in range(2)]
     toks = torch.empty((wl.n, wl.bls), dtype=torch.int32, device=dev)   # generated, time-major
 
-    def step(evs=None, prompt_ids=prompt):
+    graphs = []
+
+    def step(evs=None, prompt_ids=prompt, eager=False):
         # greedy generation of n tokens per prompt: token 1 from the prefill,
-        # token t+1 from decode step t fed token t; all on the device
+        # token t+1 from decode step t fed token t; all on the device.  The
+        # decode steps replay their CUDA graphs unless eager (the traced pass
+        # times every launch from the host).
         if evs:
             evs[0].record(stream)
         lg = model.prefill(prompt_ids, args.order, logits=logits_buf[0])
         fg.fg_argmax(lg, out=toks[0])
         if evs:
             evs[1].record(stream)
-        for t in range(1, D + 1):
-            lg = model.decode_step(toks[t - 1], t, wl.s, args.order, logits=logits_buf[t % 2])
-            fg.fg_argmax(lg, out=toks[t])
+        if graphs and not eager:
+            for gph in graphs:
+                gph.replay()
+        else:
+            for t in range(1, D + 1):
+                lg = model.decode_step(toks[t - 1], t, wl.s, args.order, logits=logits_buf[t % 2])
+                fg.fg_argmax(lg, out=toks[t])
         if evs:
             evs[2].record(stream)
 
     for _ in range(args.warmup):
         step()
     fg.fg_check()
+    if not args.no_graphs and not host:
+        graphs.extend(model.capture_decode_steps(toks, wl.s, logits_buf, args.order))
+        step()
+        fg.fg_check()
 
     # ---------------- timed region (device-resident inputs).  K steps timed
     # with one event pair per phase give the throughput; K more steps with an
@@ -301,7 +313,7 @@ def run_fg(args, ws, rank, local):
     fg.fg_trace_begin(fg.FG_TRACE_GEMM_PREFILL | fg.FG_TRACE_GEMM_DECODE |
                       fg.FG_TRACE_ATTN_DECODE | fg.FG_TRACE_ATTN_PREFILL)
     for k in range(args.steps):
-        step()
+        step(eager=True)
     torch.cuda.synchronize()
     trace = fg.fg_trace_end()
     barrier()
@@ -405,6 +417,7 @@ def run_fg(args, ws, rank, local):
                    "decode_attention": ("top-K sparse, %d%% of the rows' V" % args.topk
                                         if 0 < args.topk < 100 else "dense"),
                    "order": args.order, "decoding": "greedy (argmax on the device)",
+                   "decode_launch": "one CUDA graph per decode step" if graphs else "eager",
                    "parallelism": "replicas" if ws > 1 else "single",
                    "weights": ("4-bit, pinned host memory, streamed one layer ahead over "
                                "NVLink-C2C" if host else "4-bit, resident in HBM"),
@@ -701,29 +714,51 @@ def run_layer_workload(args, wl, local):
     y_dec = torch.empty_like(x_dec)
     order = fg.FG_ORDER_BLOCK
 
-    def step(evs=None, xp=x_pre, xd=x_dec):
+    graphs = []
+
+    def step(evs=None):
         if evs:
             evs[0].record(stream)
-        stack.run(xp, fg.FG_PHASE_PREFILL, wl.s, 0, order, out=y_pre)
+        stack.run(x_pre, fg.FG_PHASE_PREFILL, wl.s, 0, order, out=y_pre)
         if evs:
             evs[1].record(stream)
-        for t in range(1, D + 1):
-            stack.run(xd[t - 1], fg.FG_PHASE_DECODE, 1, wl.s + t - 1, order, out=y_dec[t - 1])
+        if graphs:
+            for gph in graphs:
+                gph.replay()
+        else:
+            for t in range(1, D + 1):
+                stack.run(x_dec[t - 1], fg.FG_PHASE_DECODE, 1, wl.s + t - 1, order, out=y_dec[t - 1])
         if evs:
             evs[2].record(stream)
 
     for _ in range(args.warmup):
         step()
     fg.fg_check()
+    launches_eager = 0
+    fg.fg_trace_begin(0)
+    step()
+    torch.cuda.synchronize()
+    launches_eager = sum(c["launches"] for c in fg.fg_trace_end().values())
+    if not args.no_graphs:
+        # one CUDA graph per decode step (its slot is a launch argument)
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        for t in range(1, D + 1):
+            gph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gph, stream=side):
+                stack.run(x_dec[t - 1], fg.FG_PHASE_DECODE, 1, wl.s + t - 1, order, out=y_dec[t - 1],
+                          stream=side)
+            graphs.append(gph)
+        stream.wait_stream(side)
+        step()
+        fg.fg_check()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     torch.cuda.synchronize()
     clocks.start()
-    fg.fg_trace_begin(0)
     for k in range(args.steps):
         step(evs[k])
     torch.cuda.synchronize()
-    trace = fg.fg_trace_end()
     clk = clocks.stop()
     fg.fg_check()
     t_pre = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3
@@ -736,15 +771,14 @@ def run_layer_workload(args, wl, local):
         h_pre = x_pre.cpu().pin_memory()
         h_dec = x_dec.cpu().pin_memory()
         h_out = torch.empty_like(y_dec[-1], device="cpu").pin_memory()
-        d_pre, d_dec = torch.empty_like(x_pre), torch.empty_like(x_dec)
         tot_dec = 0.0
         for k in range(args.steps):
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
             ev[0].record(stream)
-            d_pre.copy_(h_pre, non_blocking=True)
-            d_dec.copy_(h_dec, non_blocking=True)
+            x_pre.copy_(h_pre, non_blocking=True)
+            x_dec.copy_(h_dec, non_blocking=True)
             ev[1].record(stream)
-            step(ev[2:5], xp=d_pre, xd=d_dec)
+            step(ev[2:5])
             h_out.copy_(y_dec[-1], non_blocking=True)
             ev[5].record(stream)
             torch.cuda.synchronize()
@@ -778,10 +812,11 @@ def run_layer_workload(args, wl, local):
             "config": {"workload": "%s: one decoder layer, h1 %d, %d heads, h2 %d; gbs %d x k %d, "
                                    "s %d, %d teacher-forced decode steps; weights and KV 4-bit g64"
                                    % (wl.name, wl.h1, wl.H, wl.h2, wl.gbs, wl.k, wl.s, D),
+                       "decode_launch": "one CUDA graph per decode step" if graphs else "eager",
                        "l2": "inputs smaller than L2 (a latency-bound workload; no flush)"},
             "phase_ms_per_step": {"prefill": t_pre / args.steps * 1e3,
                                   "decode": t_dec / args.steps * 1e3},
-            "gpu_launches": int(sum(c["launches"] for c in trace.values())),
+            "gpu_launches": int(launches_eager) * args.steps,
             "cpu_baseline": cpu_base, "e2e": e2e, "clocks": clk}
 
 
@@ -830,6 +865,8 @@ def main(argv=None):
     ap.add_argument("--cpu-frac", type=int, default=1)
     ap.add_argument("--ref-frac", type=int, default=4)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graphs", action="store_true",
+                    help="launch the decode steps eagerly instead of replaying CUDA graphs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gbs", type=int, default=0, help="--micro decode: override gbs")
     ap.add_argument("--k", type=int, default=0, help="--micro decode: override k")

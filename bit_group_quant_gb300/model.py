@@ -171,6 +171,31 @@ class Model:
                            pad=pad)
         return self.head(y, ids.shape[0], self.stack.h1, logits=logits, stream=stream)
 
+    def capture_decode_steps(self, toks, s, logits, order="block", pad=None, steps=None):
+        """One CUDA graph per greedy decode step t = 1..D (D = toks.shape[0]-1,
+        or `steps`): the embedding of toks[t-1] at slot s+t-1, every layer
+        step, the final LayerNorm, the LM head into logits[t % 2] and
+        fg_argmax into toks[t] -- the launches decode_step and fg_argmax make,
+        recorded once and replayed without host work.  A step's slot (pos) is
+        a launch argument, so each step has its own graph.  Replays compute
+        exactly what the eager calls compute (same kernels, arguments and
+        buffers); the workspaces must already exist (run one eager step
+        first).  HBM-resident weights only."""
+        if isinstance(self.stack, HostLayerStack):
+            raise ValueError("decode graphs need the HBM-resident stack")
+        D = toks.shape[0] - 1 if steps is None else steps
+        graphs = []
+        side = torch.cuda.Stream(toks.device)
+        side.wait_stream(torch.cuda.current_stream(toks.device))
+        for t in range(1, D + 1):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                lg = self.decode_step(toks[t - 1], t, s, order, logits=logits[t % 2], pad=pad)
+                fg.fg_argmax(lg, out=toks[t])
+            graphs.append(g)
+        torch.cuda.current_stream(toks.device).wait_stream(side)
+        return graphs
+
     def generate(self, prompt_ids, decode_ids_tm, order="block", stream=None, pad=None):
         """Teacher-forced generation.  prompt_ids: int32 [bls][s]; decode_ids_tm:
         int32 [D][bls] (time-major, row t-1 fed at decode step t).  Returns
