@@ -1425,6 +1425,7 @@ fg_status launch_decode_attn_topk(const __half* qkv, int64_t ld, const fg_kv4* c
 fg_status launch_prefill_attn(const __half* qkv, int32_t B, int32_t s, int32_t H, int32_t d,
                               const int32_t* pad, __half* out, cudaStream_t st) {
     if (B == 0 || s == 0) return FG_OK;
+    if (prefill_attn_tc_supported(d)) return launch_prefill_attn_tc(qkv, B, s, H, d, pad, out, st);
     dim3 grid(static_cast<unsigned>(cdiv(s, kFaM)), H, B);
     const double bh = static_cast<double>(B) * H;
     TraceScope ts(FG_TRACE_ATTN_PREFILL, st, 2.0 * bh * s * (s + 1.0) * d,

@@ -82,6 +82,10 @@ fg_status launch_decode_attn_f16(const __half* qkv, int64_t ld, const fg_kv16* c
                                  cudaStream_t st);
 fg_status launch_prefill_attn(const __half* qkv, int32_t B, int32_t s, int32_t H, int32_t d,
                               const int32_t* pad, __half* out, cudaStream_t st);
+// attn_tc.cu: the same causal prefill attention on tcgen05 (d 64 or 128).
+bool prefill_attn_tc_supported(int32_t d);
+fg_status launch_prefill_attn_tc(const __half* qkv, int32_t B, int32_t s, int32_t H, int32_t d,
+                                 const int32_t* pad, __half* out, cudaStream_t st);
 
 struct GemmPlan {
     int nt;          // activation rows per tile (MMA N), multiple of 16, <= 256
