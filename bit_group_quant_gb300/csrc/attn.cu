@@ -1073,206 +1073,6 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     }
 }
 
-// Causal prefill attention on the tensor cores (flash-attention forward):
-// one CTA of 4 warps per (64-query block, head, sequence), 16 queries per
-// warp; 64-key tiles of K and V double-buffered in shared memory by cp.async
-// (16-byte chunks XOR-swizzled by row so ldmatrix is conflict-free);
-// S = Q K^T and O += P V on mma.sync m16n8k16 (fp16 in, fp32 accumulate) with
-// an online softmax in fp32 (P enters the second product as fp16).  Key tiles
-// beyond the block's last query are skipped; the diagonal tile is masked.
-// Query blocks are visited heaviest first.  A left-padded sequence is
-// computed as its real part alone: query and key tiles start at its first
-// real slot p0 (Q/K/V and output rows shifted by p0), so every real row is
-// bit-identical to the same prompt run unpadded; block qb also zeroes the
-// padding rows [64 qb, 64 qb + 64) below p0.
-constexpr int kFaM = 64;   // queries per CTA
-constexpr int kFaN = 64;   // keys per tile
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-template <int D>
-__global__ void __launch_bounds__(128) prefill_attn_fa_kernel(const __half* __restrict__ qkv,
-                                                              int32_t s_all, int32_t H,
-                                                              const int32_t* __restrict__ pad,
-                                                              __half* __restrict__ out_all) {
-    constexpr int CH = D / 8;                 // 16-byte chunks per row
-    constexpr int TB = kFaN * D * 2;          // bytes of one K or V tile
-    constexpr int KS = D / 16;                // k-steps of Q K^T
-    constexpr int NT = D / 8;                 // n-tiles of the output
-    extern __shared__ __align__(128) uint8_t fsm[];
-    const uint32_t sQ = smem_u32(fsm), sK = sQ + kFaM * D * 2, sV = sK + 2 * TB;
-    const int nqb = (s_all + kFaM - 1) / kFaM;
-    const int qb = nqb - 1 - static_cast<int>(blockIdx.x);   // heaviest first
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int64_t h1 = static_cast<int64_t>(H) * D, ld = 3 * h1;
-    // first real slot (a padding count outside [0, s_all) is clamped)
-    const int p0 = pad ? min(max(pad[b], 0), s_all - 1) : 0;
-    // output row r of the sequence (slot r), this head
-    auto out_row = [&](int r) {
-        return out_all + (static_cast<int64_t>(b) * s_all + r) * h1 + static_cast<int64_t>(h) * D;
-    };
-    for (int i = threadIdx.x; i < kFaM * CH; i += 128) {   // padding rows of this block: zeros
-        const int row = qb * kFaM + i / CH;
-        if (row < p0) *reinterpret_cast<uint4*>(out_row(row) + (i % CH) * 8) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    // the real part: s rows starting at slot p0
-    const int s = s_all - p0;
-    const int q0 = qb * kFaM;
-    if (q0 >= s) return;
-    const __half* base = qkv + (static_cast<int64_t>(b) * s_all + p0) * ld +
-                         static_cast<int64_t>(h) * D;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
-    // swizzled byte offset of (row, 16-byte chunk) inside a [rows][D] fp16 tile
-    auto swz = [](int r, int c) { return static_cast<uint32_t>(r * D * 2 + ((c ^ (r & 7)) << 4)); };
-    // one [64][D] tile of rows r0.. of block `part` (0 q, 1 k, 2 v); rows past s read as zeros
-    auto load_tile = [&](uint32_t dst, int part, int r0) {
-        for (int i = threadIdx.x; i < 64 * CH; i += 128) {
-            const int r = i / CH, c = i % CH;
-            const int row = r0 + r;
-            const bool ok = row < s;
-            const __half* src = base + static_cast<int64_t>(ok ? row : 0) * ld + part * h1 + c * 8;
-            cp_async16(dst + swz(r, c), src, ok ? 16u : 0u);
-        }
-    };
-    const int ntiles = min((q0 + kFaM - 1) / kFaN + 1, (s + kFaN - 1) / kFaN);
-    load_tile(sQ, 0, q0);
-    load_tile(sK, 1, 0);
-    load_tile(sV, 2, 0);
-    cp_async_commit();
-
-    const float sl2 = __fdiv_rn(1.0f, __fsqrt_rn(static_cast<float>(D))) * 1.4426950408889634f;
-    float o[NT][4];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
-    float mrow[2] = {-CUDART_INF_F, -CUDART_INF_F}, lrow[2] = {0.0f, 0.0f};
-    uint32_t qf[KS][4];
-    const int qr0 = warp * 16;   // this warp's rows in the block
-
-    for (int j = 0; j < ntiles; ++j) {
-        const int buf = j & 1;
-        if (j + 1 < ntiles) {   // prefetch the next tile into the other buffer
-            load_tile(sK + (buf ^ 1) * TB, 1, (j + 1) * kFaN);
-            load_tile(sV + (buf ^ 1) * TB, 2, (j + 1) * kFaN);
-        }
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        if (j == 0) {
-#pragma unroll
-            for (int kk = 0; kk < KS; ++kk)
-                ldsm_x4(sQ + swz(qr0 + (lane & 15), 2 * kk + (lane >> 4)), qf[kk][0], qf[kk][1],
-                        qf[kk][2], qf[kk][3]);
-        }
-        const uint32_t kb = sK + buf * TB, vb = sV + buf * TB;
-        // ---- S = Q K^T for 64 keys: 8 n-tiles
-        float sacc[8][4];
-#pragma unroll
-        for (int n = 0; n < 8; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.0f;
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {   // two n-tiles per ldmatrix.x4
-                uint32_t b0, b1, b2, b3;
-                const int key = np * 16 + (lane & 7) + 8 * (lane >> 4);
-                ldsm_x4(kb + swz(key, 2 * kk + ((lane >> 3) & 1)), b0, b1, b2, b3);
-                mma16816(sacc[2 * np], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
-                mma16816(sacc[2 * np + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
-            }
-        }
-        // ---- online softmax (log2 domain); mask keys past the query on the diagonal tile
-        const bool diag = (j + 1) * kFaN > q0 + qr0;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int qi = q0 + qr0 + g + 8 * r;
-            float mx = -CUDART_INF_F;
-#pragma unroll
-            for (int n = 0; n < 8; ++n)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float v = sacc[n][2 * r + e] * sl2;
-                    if (diag && j * kFaN + 8 * n + 2 * t + e > qi) v = -CUDART_INF_F;
-                    sacc[n][2 * r + e] = v;
-                    mx = fmaxf(mx, v);
-                }
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float mnew = fmaxf(mrow[r], mx);
-            // a row with no visible key yet keeps m = -inf; avoid inf - inf
-            const float corr = mnew == -CUDART_INF_F ? 1.0f : exp2f(mrow[r] - mnew);
-            float ps = 0.0f;
-#pragma unroll
-            for (int n = 0; n < 8; ++n)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float v = sacc[n][2 * r + e];
-                    const float pv = v == -CUDART_INF_F ? 0.0f : exp2f(v - mnew);
-                    sacc[n][2 * r + e] = pv;
-                    ps += pv;
-                }
-            lrow[r] = lrow[r] * corr + ps;
-            mrow[r] = mnew;
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                o[n][2 * r] *= corr;
-                o[n][2 * r + 1] *= corr;
-            }
-        }
-        // ---- O += P V: P from the S registers (fp16), 4 k-steps of 16 keys
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t a0 = pack_h2(sacc[2 * kk][0], sacc[2 * kk][1]);
-            const uint32_t a1 = pack_h2(sacc[2 * kk][2], sacc[2 * kk][3]);
-            const uint32_t a2 = pack_h2(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
-            const uint32_t a3 = pack_h2(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
-#pragma unroll
-            for (int dp = 0; dp < NT / 2; ++dp) {   // two output n-tiles per ldmatrix.x4.trans
-                uint32_t b0, b1, b2, b3;
-                const int key = 16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1);
-                ldsm_x4_t(vb + swz(key, 2 * dp + (lane >> 4)), b0, b1, b2, b3);
-                mma16816(o[2 * dp], a0, a1, a2, a3, b0, b1);
-                mma16816(o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
-            }
-        }
-        __syncthreads();   // the buffer of tile j is refilled next iteration
-    }
-    // ---- row sums over the 4 lanes of a row, normalise, store fp16
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        float lsum = lrow[r];
-        lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
-        lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
-        const int qi = q0 + qr0 + g + 8 * r;
-        if (qi < s) {
-            const float inv = 1.0f / lsum;
-            __half* orow = out_row(p0 + qi);
-#pragma unroll
-            for (int n = 0; n < NT; ++n)
-                *reinterpret_cast<uint32_t*>(orow + 8 * n + 2 * t) =
-                    pack_h2(o[n][2 * r] * inv, o[n][2 * r + 1] * inv);
-        }
-    }
-}
 
 // Dynamic shared memory a block may use (227 KB less the kernels' static arrays).
 constexpr size_t kMaxDynSmem = 220 * 1024;
@@ -1425,26 +1225,9 @@ fg_status launch_decode_attn_topk(const __half* qkv, int64_t ld, const fg_kv4* c
 fg_status launch_prefill_attn(const __half* qkv, int32_t B, int32_t s, int32_t H, int32_t d,
                               const int32_t* pad, __half* out, cudaStream_t st) {
     if (B == 0 || s == 0) return FG_OK;
-    if (prefill_attn_tc_supported(d)) return launch_prefill_attn_tc(qkv, B, s, H, d, pad, out, st);
-    dim3 grid(static_cast<unsigned>(cdiv(s, kFaM)), H, B);
-    const double bh = static_cast<double>(B) * H;
-    TraceScope ts(FG_TRACE_ATTN_PREFILL, st, 2.0 * bh * s * (s + 1.0) * d,
-                  bh * s * d * 2.0 * 4.0);
-    const size_t smem = static_cast<size_t>(kFaM) * d * 2 + 4 * static_cast<size_t>(kFaN) * d * 2;
-    if (d == 64) {
-        auto kern = prefill_attn_fa_kernel<64>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return cuda_error(e, "prefill_attn smem attribute");
-        kern<<<grid, 128, smem, st>>>(qkv, s, H, pad, out);
-    } else {
-        auto kern = prefill_attn_fa_kernel<128>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return cuda_error(e, "prefill_attn smem attribute");
-        kern<<<grid, 128, smem, st>>>(qkv, s, H, pad, out);
-    }
-    return cuda_error(cudaGetLastError(), "prefill_attn launch");
+    if (!prefill_attn_tc_supported(d))
+        return set_error(FG_ERR_UNSUPPORTED, "prefill_attn: head dim %d not in {64, 128}", d);
+    return launch_prefill_attn_tc(qkv, B, s, H, d, pad, out, st);
 }
 
 }  // namespace fg
