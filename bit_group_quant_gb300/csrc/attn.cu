@@ -323,6 +323,11 @@ __global__ void __launch_bounds__(32) topk_gather_kernel(
     int32_t cap, int32_t pos, const int32_t* __restrict__ pad, int32_t keep_pct, int32_t kmax,
     const uint8_t* __restrict__ v_codes, const float* __restrict__ v_meta,
     __half* __restrict__ out, int32_t* __restrict__ sel_out) {
+    // the inputs come from earlier kernels of the stream (this launch may
+    // start before they finish): wait for them, then let the next kernel be
+    // scheduled
+    griddep_wait();
+    griddep_launch();
     constexpr int G = D / 64, RB = D / 2, RS = tk_row_bytes<D>(), DPL = D / 32;
     extern __shared__ __align__(128) uint8_t dyn[];
     const int lane = threadIdx.x;
@@ -485,6 +490,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
     const int32_t* __restrict__ pad, int32_t fuse_append, uint8_t* k_codes, uint8_t* v_codes,
     float* k_meta, float* v_meta, __half* __restrict__ out, float* __restrict__ sc_out,
     float* __restrict__ st_out, int32_t sc_ld) {
+    // the inputs come from earlier kernels of the stream (this launch may
+    // start before they finish): wait for them, then let the next kernel be
+    // scheduled
+    griddep_wait();
+    griddep_launch();
     constexpr int G = D / 64;            // groups per head row
     constexpr int RB = D / 2;            // code bytes per row
     constexpr int WPT = D / 32;          // code words per lane per row in pass 1
@@ -746,6 +756,11 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
     float* k_meta, float* v_meta, __half* __restrict__ out, int* status,
     unsigned long long wait_ns, float* __restrict__ sc_out, float* __restrict__ st_out,
     int32_t sc_ld) {
+    // the inputs come from earlier kernels of the stream (this launch may
+    // start before they finish): wait for them, then let the next kernel be
+    // scheduled
+    griddep_wait();
+    griddep_launch();
     constexpr int D = 128, G = 2, RB = kRB128, WPT = D / 32, NX = 2 * WPT;
     constexpr int NWARP = kDecThreads / 32;
     extern __shared__ __align__(128) uint8_t dyn[];
@@ -1127,9 +1142,13 @@ fg_status launch_decode_t(const __half* qkv, int64_t ld, const fg_kv4* c, int32_
     const double bh = static_cast<double>(c->B) * c->H;
     fg::TraceScope ts(FG_TRACE_ATTN_DECODE, st, (SCORES ? 2.0 : 4.0) * bh * L * D,
                       decode_attn_bytes(D, bh, L, SCORES ? 0 : L, fuse_append != 0));
-    kern<<<grid, kDecThreads, smem, st>>>(qkv, ld, c->H, c->cap, pos, pad, fuse_append,
+    {
+        const cudaError_t le_ = fg::launch_pdl(kern, dim3(grid), dim3(kDecThreads), smem, st,
+            qkv, ld, c->H, c->cap, pos, pad, fuse_append,
                                           c->k_codes, c->v_codes, c->k_meta, c->v_meta, out,
                                           w.sc, w.st, w.sc_ld);
+        if (le_ != cudaSuccess) return fg::cuda_error(le_, "kern launch");
+    }
     return fg::cuda_error(cudaGetLastError(), "decode_attn launch");
 }
 
@@ -1151,10 +1170,14 @@ fg_status launch_decode_staged(const __half* qkv, int64_t ld, const fg_kv4* c, i
     const double bh = static_cast<double>(c->B) * c->H;
     fg::TraceScope ts(FG_TRACE_ATTN_DECODE, st, (SCORES ? 2.0 : 4.0) * bh * L * D,
                       decode_attn_bytes(D, bh, L, SCORES ? 0 : L, fuse_append != 0));
-    kern<<<grid, kDecThreads, smem, st>>>(qkv, ld, c->H, c->cap, pos, pad, fuse_append,
+    {
+        const cudaError_t le_ = fg::launch_pdl(kern, dim3(grid), dim3(kDecThreads), smem, st,
+            qkv, ld, c->H, c->cap, pos, pad, fuse_append,
                                           c->k_codes, c->v_codes, c->k_meta, c->v_meta, out,
                                           fg::device_status_ptr(), fg::wait_limit_ns(), w.sc, w.st,
                                           w.sc_ld);
+        if (le_ != cudaSuccess) return fg::cuda_error(le_, "kern launch");
+    }
     return fg::cuda_error(cudaGetLastError(), "decode_attn launch");
 }
 
@@ -1178,9 +1201,11 @@ fg_status launch_topk_gather(const fg_kv4* c, int32_t pos, const int32_t* pad, i
     const double row = D / 2 + (D / 64) * 8.0;
     fg::TraceScope ts(FG_TRACE_ATTN_DECODE, st, 2.0 * units * kmax * D,
                       static_cast<double>(units) * (kmax * row + D * 2.0));
-    kern<<<static_cast<unsigned>(units), 32, smem, st>>>(w.sc, w.st, w.sc_ld, c->H, c->cap, pos, pad,
-                                                          keep_pct, kmax, c->v_codes, c->v_meta,
-                                                          out, sel_out);
+    {
+        const cudaError_t le_ = fg::launch_pdl(kern, dim3(static_cast<unsigned>(units)), dim3(32), smem, st,
+            w.sc, w.st, w.sc_ld, c->H, c->cap, pos, pad, keep_pct, kmax, c->v_codes, c->v_meta, out, sel_out);
+        if (le_ != cudaSuccess) return fg::cuda_error(le_, "kern launch");
+    }
     return fg::cuda_error(cudaGetLastError(), "topk_gather launch");
 }
 

@@ -28,6 +28,11 @@ __global__ void kv_store_f16_kernel(const __half* __restrict__ qkv, int64_t ld, 
                                     int32_t H, int32_t d, int32_t cap, int32_t slot0,
                                     __half* __restrict__ k, __half* __restrict__ v,
                                     int64_t nvec) {
+    // the inputs come from earlier kernels of the stream (this launch may
+    // start before they finish): wait for them, then let the next kernel be
+    // scheduled
+    griddep_wait();
+    griddep_launch();
     // vector i: row r = i / (2 h1 / 8), then k/v and the 8 values within
     const int64_t h1 = static_cast<int64_t>(H) * d;
     const int64_t per_row = 2 * h1 / 8;
@@ -75,6 +80,11 @@ __global__ void __launch_bounds__(kThreads) decode_attn_f16_kernel(
     const __half* __restrict__ qkv, int64_t ld, int32_t H, int32_t cap, int32_t pos,
     const int32_t* __restrict__ pad, int32_t fuse_append, __half* kc, __half* vc,
     __half* __restrict__ out, int* status, unsigned long long wait_ns) {
+    // the inputs come from earlier kernels of the stream (this launch may
+    // start before they finish): wait for them, then let the next kernel be
+    // scheduled
+    griddep_wait();
+    griddep_launch();
     constexpr int LPR = D / 8;          // lanes per row
     constexpr int RPI = 32 / LPR;       // rows per warp per step
     constexpr int RB = D * 2;           // bytes per row
@@ -257,9 +267,11 @@ fg_status launch_kv_store_f16(const __half* qkv, int64_t ld, int32_t T, const fg
     const int threads = 256;
     const int64_t blocks = std::min<int64_t>(cdiv(nvec, threads), 64LL * num_sms());
     TraceScope ts(FG_TRACE_OTHER, st, 0.0, 2.0 * nvec * 16);
-    kv_store_f16_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
-        qkv, ld, T, c->H, c->d, c->cap, slot0, reinterpret_cast<__half*>(c->k),
-        reinterpret_cast<__half*>(c->v), nvec);
+    {
+        const cudaError_t le_ = fg::launch_pdl(kv_store_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st,
+            qkv, ld, T, c->H, c->d, c->cap, slot0, reinterpret_cast<__half*>(c->k), reinterpret_cast<__half*>(c->v), nvec);
+        if (le_ != cudaSuccess) return fg::cuda_error(le_, "kv_store_f16_kernel launch");
+    }
     return cuda_error(cudaGetLastError(), "kv_store_f16 launch");
 }
 
@@ -282,10 +294,14 @@ static fg_status launch_decode_f16_t(const __half* qkv, int64_t ld, const fg_kv1
     const double bh = static_cast<double>(c->B) * c->H;
     TraceScope ts(FG_TRACE_ATTN_DECODE, st, 4.0 * bh * L * D,
                   bh * (2.0 * L * D * 2 + (fuse_append ? 2.0 * D * 2 : 0.0) + 3.0 * D * 2 + D * 2));
-    kern<<<grid, kThreads, smem, st>>>(qkv, ld, c->H, c->cap, pos, pad, fuse_append,
+    {
+        const cudaError_t le_ = fg::launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st,
+            qkv, ld, c->H, c->cap, pos, pad, fuse_append,
                                        reinterpret_cast<__half*>(c->k),
                                        reinterpret_cast<__half*>(c->v), out, device_status_ptr(),
                                        wait_limit_ns());
+        if (le_ != cudaSuccess) return fg::cuda_error(le_, "kern launch");
+    }
     return cuda_error(cudaGetLastError(), "decode_attn_f16 launch");
 }
 

@@ -106,6 +106,11 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm, int32_t s_all, int32_t H,
                            int32_t B, const int32_t* __restrict__ pad, __half* __restrict__ out_all,
                            int* status, unsigned long long wait_ns) {
+    // the inputs come from earlier kernels of the stream (this launch may
+    // start before they finish): wait for them, then let the next kernel be
+    // scheduled
+    griddep_wait();
+    griddep_launch();
     constexpr int NB = D / 64;                     // 64-dim boxes per tile
     constexpr uint32_t kTile = NB * kBoxBytes;     // bytes of Q, K or V
     extern __shared__ uint8_t smem_raw[];
@@ -437,9 +442,11 @@ fg_status launch_tc(const CUtensorMap& tm, int32_t B, int32_t s, int32_t H, cons
     const int64_t items = fg::cdiv(s, kBQ) * H * static_cast<int64_t>(B);
     int64_t grid = 2 * static_cast<int64_t>(fg::num_sms()) - 1;
     if (grid > items) grid = items;
-    kern<<<static_cast<unsigned>(grid), kThreadsT, smem, st>>>(tm, s, H, B, pad, out,
-                                                               fg::device_status_ptr(),
-                                                               fg::wait_limit_ns());
+    {
+        const cudaError_t le_ = fg::launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreadsT), smem, st,
+            tm, s, H, B, pad, out, fg::device_status_ptr(), fg::wait_limit_ns());
+        if (le_ != cudaSuccess) return fg::cuda_error(le_, "kern launch");
+    }
     return fg::cuda_error(cudaGetLastError(), "prefill_attn_tc launch");
 }
 

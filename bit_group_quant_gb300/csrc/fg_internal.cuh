@@ -124,6 +124,41 @@ bool plan_gemm_dec(int64_t M, int64_t N, int64_t K, int64_t plan_rows, GemmPlan&
 fg_status launch_gemm_dec(const __half* X, int64_t M, const fg_q4* W, const __half* bias,
                           const __half* residual, int act, __half* Y, void* ws, size_t ws_bytes,
                           cudaStream_t st, const GemmPlan& pl);
+// Programmatic dependent launch.  Every kernel of a layer step is launched
+// with programmatic stream serialization: it may be scheduled while the
+// kernel before it in the stream is still running, so its set-up (barriers,
+// TMEM, tensor-map prefetch) and its reads of data no earlier kernel writes
+// (the 4-bit weights) overlap that kernel's tail.  Each kernel signals
+// griddep_launch() early and calls griddep_wait() before its first access to
+// memory that an earlier kernel writes or reads.  The next kernel is
+// scheduled only after every CTA of this one has started, so a grid whose
+// CTAs wait on one another (all co-resident) is never starved by it.
+// (Launched without the attribute, or after a non-kernel stream operation,
+// the wait returns at once and the signal has no effect.)
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+// Adds the programmatic-serialization attribute to a launch configuration
+// that already carries `n` attributes in `attr` (room for one more).
+inline void add_pdl_attr(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int n) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = n + 1;
+}
+
 // 2-D row-major tensor map [rows][cols] of `esize`-byte elements, box {bx, by}.
 fg_status make_tmap(CUtensorMap* tm, const void* ptr, CUtensorMapDataType dt, int esize,
                     uint64_t cols, uint64_t rows, uint32_t bx, uint32_t by,
@@ -149,6 +184,14 @@ __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// Programmatic dependent launch (see fg::launch_pdl): wait until every
+// earlier kernel of the stream has completed and its memory is visible;
+// allow the next kernel to be scheduled.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void report(int* status, int code) {

@@ -184,6 +184,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto chunk_at = [&](int i) { return kc0 + (i + rot) % nk; };
     const uint32_t ncols = p.nt <= 32 ? 32u : (p.nt <= 64 ? 64u : (p.nt <= 128 ? 128u : 256u));
     const uint64_t lim = p.wait_ns;
+    // The weight side (4-bit codes and (min, scale), or the fp16 token
+    // embedding of the LM head) never changes during a step: it is fetched
+    // and dequantised at once, possibly while the previous kernel of the
+    // stream still runs; the activation producer and the epilogue first wait
+    // for that kernel.
+    griddep_launch();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < sm.ns; ++s) {
@@ -281,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // ---------------- activation TMA producer: this CTA's 1/c slice of
             // each B tile, multicast to every CTA of the cluster
+            griddep_wait();
             const int srows = p.nt / ccount;
             const uint32_t soff = crank * static_cast<uint32_t>(srows) * 128u;
             int issued_last[kMaxStages];
@@ -442,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Lanes may leave the backed-off wait at different times: __all_sync
         // makes the outcome uniform and reconverges the warp before the
         // .sync.aligned TMEM loads below.
+        griddep_wait();
         const bool ok = __all_sync(0xffffffffu, mbar_wait_sleepy(sm.acc(), 0, lim));
         if (!ok && lane == 0) report(p.status, fg::kDevTimeout);
         tc_fence_after();
@@ -511,6 +519,11 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
                                                             const __half* __restrict__ bias,
                                                             const __half* __restrict__ residual,
                                                             int act, __half* __restrict__ Y) {
+    // the inputs come from earlier kernels of the stream (this launch may
+    // start before they finish): wait for them, then let the next kernel be
+    // scheduled
+    griddep_wait();
+    griddep_launch();
     const int64_t nv = M * N / 4;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nv;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -596,13 +609,12 @@ fg_status run_gemm(const void* X, const CUtensorMap& tmW, GemmParams& p, const f
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = rg.smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = p.cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    fg::add_pdl_attr(cfg, attr, 1);
     const double M = p.M, N = p.N, K = p.K;
     // algorithmic traffic: the weight once (4-bit codes + fp32 (min, scale) per
     // 64, or fp16), X once, Y once (+ residual, or fp32 partials / logits)
@@ -748,8 +760,11 @@ fg_status launch_gemm_g4(const __half* X, int64_t M, const fg_q4* W, const __hal
     int64_t blocks = cdiv(nv, 256);
     if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
     TraceScope ts(FG_TRACE_OTHER, st, 0.0, pl.splits * M * N * 4.0 + M * N * 4.0);
-    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        p.partial, pl.splits, M, N, bias, residual, act, Y);
+    {
+        const cudaError_t le_ = fg::launch_pdl(splitk_reduce_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+            p.partial, pl.splits, M, N, bias, residual, act, Y);
+        if (le_ != cudaSuccess) return fg::cuda_error(le_, "splitk_reduce_kernel launch");
+    }
     return cuda_error(cudaGetLastError(), "splitk reduce launch");
 }
 

@@ -179,6 +179,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     proto.nbox = p.nbox;
     const int nstages = static_cast<int>(2 * (proto.hi - proto.u));
     const uint64_t lim = p.wait_ns;
+    // The weights (codes and (min, scale)) never change during a step: their
+    // loads and dequantisation start at once, possibly while the previous
+    // kernel of the stream still runs; the roles that read activations,
+    // residuals, partial sums or flags, or write Y, first wait for it.
+    griddep_launch();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNS; ++s) {
@@ -353,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // ---------------- activation TMA producer: this CTA's 1/c slice of
             // the rows of each stage (both 64-k halves), multicast to the cluster
+            griddep_wait();
             const int srows = p.nt / c;
             const uint32_t soff = crank * static_cast<uint32_t>(srows) * 128u;
             int issued_last[kNS];
@@ -514,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dequantisers, idle by then, share it with the epilogue warp of
         // their lane quarter (8-column chunks 1 + g, 5 + g, ...).
         if (!failed) {
+            griddep_wait();
             SegIter it = proto;
             int nseg = 0, lt = 0, lb0 = 0, lb1 = 0;
             while (it.next()) {
@@ -541,6 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 4) {
         // ---------------- epilogue, warps 4-7 = TMEM lane quarters 0-3
+        griddep_wait();
         const int qq = warp & 3;
         const int row = qq * 32 + lane;
         const uint32_t tl = static_cast<uint32_t>(qq * 32) << 16;
@@ -733,13 +741,12 @@ fg_status launch_gemm_dec(const __half* X, int64_t M, const fg_q4* W, const __ha
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = c;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    fg::add_pdl_attr(cfg, attr, 1);
     const double Md = M, Nd = N, Kd = K;
     // algorithmic traffic: the weight once (codes + (min, scale)), X once, Y once
     // (+ residual); the partial sums of split tiles stay in L2

@@ -112,6 +112,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = static_cast<int>(blockIdx.x) >> 1;    // pair index
     const int ntiles = q < p.tiles ? (p.tiles - 1 - q) / p.Q + 1 : 0;
     const uint64_t lim = p.wait_ns;
+    // Both operands come from earlier kernels (the weights from the
+    // dequantisation launched just before): the producer and the epilogue
+    // wait for them; the set-up below overlaps the previous kernel's tail.
+    griddep_launch();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNS; ++s) {
@@ -160,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---------------- TMA producer: this CTA's A (weight rows) and B
             // (activation rows) of every stage, counted on the even CTA's full
             // barrier, which expects the bytes of both CTAs
+            griddep_wait();
             int issued_last[kNS];
             for (int s = 0; s < kNS; ++s) issued_last[s] = -1;
             int s = 0, i = 0;
@@ -259,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = qq * 32 + lane;
         const uint32_t tl = static_cast<uint32_t>(qq * 32) << 16;
         const uint32_t empty_remote0 = mapa_shared(acc_empty(0), 0);
+        griddep_wait();
         for (int j = 0; j < ntiles; ++j) {
             const int a = j & 1;
             int f, t;
@@ -386,13 +392,12 @@ fg_status launch_gemm_pf(const __half* X, int64_t M, const __half* W16, int64_t 
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    fg::add_pdl_attr(cfg, attr, 1);
     const double Md = M, Nd = N, Kd = K;
     // algorithmic traffic: the fp16 weights once, X once, Y once (+ residual)
     TraceScope ts(FG_TRACE_GEMM_PREFILL, st, 2.0 * Md * Nd * Kd,

@@ -134,6 +134,11 @@ __global__ void __launch_bounds__(256) dequant_g4_kernel(const uint32_t* __restr
                                                          const float2* __restrict__ meta,
                                                          int64_t ngroups,
                                                          uint4* __restrict__ x) {
+    // the inputs come from earlier kernels of the stream (this launch may
+    // start before they finish): wait for them, then let the next kernel be
+    // scheduled
+    griddep_wait();
+    griddep_launch();
     const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
          t < ngroups * 8; t += nthreads) {
@@ -166,6 +171,11 @@ __global__ void __launch_bounds__(32 * kQWarps) kv_store_kernel(
     const __half* __restrict__ qkv, int64_t ld, int32_t B, int32_t T, int32_t H, int32_t d,
     int32_t cap, int32_t slot0, uint8_t* __restrict__ k_codes, uint8_t* __restrict__ v_codes,
     float* __restrict__ k_meta, float* __restrict__ v_meta) {
+    // the inputs come from earlier kernels of the stream (this launch may
+    // start before they finish): wait for them, then let the next kernel be
+    // scheduled
+    griddep_wait();
+    griddep_launch();
     __shared__ __align__(16) uint8_t stage[kQWarps][32 * kQRow];
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     uint8_t* st = stage[wib];
@@ -242,9 +252,13 @@ fg_status launch_dequant_g4(const uint8_t* codes, const float* meta, int64_t ngr
     if (ngroups == 0) return FG_OK;
     const int grid = grid_for(ngroups * 8, 256);
     TraceScope ts(trace_cls, st, 0.0, ngroups * (128.0 + 40.0));
-    dequant_g4_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(codes),
+    {
+        const cudaError_t le_ = fg::launch_pdl(dequant_g4_kernel, dim3(grid), dim3(256), 0, st,
+            reinterpret_cast<const uint32_t*>(codes),
                                             reinterpret_cast<const float2*>(meta), ngroups,
                                             reinterpret_cast<uint4*>(x));
+        if (le_ != cudaSuccess) return fg::cuda_error(le_, "dequant_g4_kernel launch");
+    }
     return cuda_error(cudaGetLastError(), "dequant_g4 launch");
 }
 
@@ -254,8 +268,12 @@ fg_status launch_kv_store(const __half* qkv, int64_t ld, int32_t B, int32_t T, i
     if (ngroups == 0) return FG_OK;
     const int grid = grid_for(ngroups, 32 * kQWarps);  // 32 groups per warp at a time
     TraceScope ts(FG_TRACE_OTHER, st, 0.0, ngroups * (128.0 + 40.0));
-    kv_store_kernel<<<grid, 32 * kQWarps, 0, st>>>(qkv, ld, B, T, H, d, c->cap, slot0, c->k_codes,
+    {
+        const cudaError_t le_ = fg::launch_pdl(kv_store_kernel, dim3(grid), dim3(32 * kQWarps), 0, st,
+            qkv, ld, B, T, H, d, c->cap, slot0, c->k_codes,
                                           c->v_codes, c->k_meta, c->v_meta);
+        if (le_ != cudaSuccess) return fg::cuda_error(le_, "kv_store_kernel launch");
+    }
     return cuda_error(cudaGetLastError(), "kv_store launch");
 }
 

@@ -32,6 +32,11 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const __half* __r
                                                                const __half* __restrict__ g,
                                                                const __half* __restrict__ b,
                                                                float eps, __half* __restrict__ y) {
+    // the inputs come from earlier kernels of the stream (this launch may
+    // start before they finish): wait for them, then let the next kernel be
+    // scheduled
+    fgd::griddep_wait();
+    fgd::griddep_launch();
     __shared__ float red[kLnThreads / 32];
     const int64_t row = blockIdx.x;
     const uint4* xr = reinterpret_cast<const uint4*>(x + row * x_ld);
@@ -108,6 +113,11 @@ __global__ void __launch_bounds__(256) embed_kernel(const int32_t* __restrict__ 
                                                     const __half* __restrict__ e_tok,
                                                     const __half* __restrict__ e_pos, int32_t h1,
                                                     __half* __restrict__ y) {
+    // the inputs come from earlier kernels of the stream (this launch may
+    // start before they finish): wait for them, then let the next kernel be
+    // scheduled
+    fgd::griddep_wait();
+    fgd::griddep_launch();
     const int64_t nvec = static_cast<int64_t>(h1) / 8;
     const int64_t total = ntok * nvec;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -148,6 +158,11 @@ __device__ __forceinline__ ValIdx better(ValIdx a, ValIdx b) {
 
 __global__ void __launch_bounds__(kArgThreads) argmax_kernel(const float* __restrict__ logits,
                                                              int64_t V, int32_t* __restrict__ out) {
+    // the inputs come from earlier kernels of the stream (this launch may
+    // start before they finish): wait for them, then let the next kernel be
+    // scheduled
+    fgd::griddep_wait();
+    fgd::griddep_launch();
     __shared__ ValIdx red[kArgThreads / 32];
     const float* row = logits + static_cast<int64_t>(blockIdx.x) * V;
     ValIdx best{-CUDART_INF_F, 0x7fffffff};
@@ -192,7 +207,11 @@ fg_status launch_layernorm(const __half* x, int64_t rows, int64_t cols, int64_t 
         return set_error(FG_ERR_UNSUPPORTED, "layernorm: cols %lld > %d", (long long)cols,
                          kLnMaxVec * 8 * kLnThreads);
     TraceScope ts(FG_TRACE_OTHER, st, 0.0, rows * cols * 4.0);
-    layernorm_kernel<<<static_cast<unsigned>(rows), kLnThreads, 0, st>>>(x, cols, x_ld, g, b, eps, y);
+    {
+        const cudaError_t le_ = fg::launch_pdl(layernorm_kernel, dim3(static_cast<unsigned>(rows)), dim3(kLnThreads), 0, st,
+            x, cols, x_ld, g, b, eps, y);
+        if (le_ != cudaSuccess) return fg::cuda_error(le_, "layernorm_kernel launch");
+    }
     return cuda_error(cudaGetLastError(), "layernorm launch");
 }
 
@@ -203,15 +222,22 @@ fg_status launch_embed(const int32_t* ids, int64_t ntok, int32_t T, int32_t pos0
     int64_t blocks = cdiv(ntok * (h1 / 8), 256);
     if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
     TraceScope ts(FG_TRACE_OTHER, st, 0.0, ntok * h1 * 6.0);
-    embed_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(ids, ntok, T, pos0, pad, e_tok,
-                                                                e_pos, h1, y);
+    {
+        const cudaError_t le_ = fg::launch_pdl(embed_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+            ids, ntok, T, pos0, pad, e_tok, e_pos, h1, y);
+        if (le_ != cudaSuccess) return fg::cuda_error(le_, "embed_kernel launch");
+    }
     return cuda_error(cudaGetLastError(), "embed launch");
 }
 
 fg_status launch_argmax(const float* logits, int64_t B, int64_t V, int32_t* out, cudaStream_t st) {
     if (B == 0) return FG_OK;
     TraceScope ts(FG_TRACE_OTHER, st, 0.0, B * V * 4.0 + B * 4.0);
-    argmax_kernel<<<static_cast<unsigned>(B), kArgThreads, 0, st>>>(logits, V, out);
+    {
+        const cudaError_t le_ = fg::launch_pdl(argmax_kernel, dim3(static_cast<unsigned>(B)), dim3(kArgThreads), 0, st,
+            logits, V, out);
+        if (le_ != cudaSuccess) return fg::cuda_error(le_, "argmax_kernel launch");
+    }
     return cuda_error(cudaGetLastError(), "argmax launch");
 }
 
