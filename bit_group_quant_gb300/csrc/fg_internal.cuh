@@ -547,6 +547,31 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, float S, float S16, float 
     return *reinterpret_cast<uint4*>(h);
 }
 
+// The same eight values with the FMAs of codes that share a multiplier
+// paired into packed fp32x2 FMAs (each half one single-rounding FMA, so the
+// result is bit-identical to dequant8): 21 instructions per word instead of
+// 25, for the kernels where the dequantisation bounds the throughput.
+__device__ __forceinline__ uint4 dequant8_x2(uint32_t w, float S, float S16, float m) {
+    const uint32_t w8 = w >> 8;
+    const uint32_t t0 = w & 0x000F000Fu, t1 = w & 0x00F000F0u;     // (c0, c4), (16c1, 16c5)
+    const uint32_t t2 = w8 & 0x000F000Fu, t3 = w8 & 0x00F000F0u;   // (c2, c6), (16c3, 16c7)
+    const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&t0));
+    const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&t1));
+    const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&t2));
+    const float2 a3 = __half22float2(*reinterpret_cast<const __half2*>(&t3));
+    const float2 SS = make_float2(S, S), S16S16 = make_float2(S16, S16), MM = make_float2(m, m);
+    const float2 r0 = __ffma2_rn(a0, SS, MM);        // (e0, e4)
+    const float2 r1 = __ffma2_rn(a1, S16S16, MM);    // (e1, e5)
+    const float2 r2 = __ffma2_rn(a2, SS, MM);        // (e2, e6)
+    const float2 r3 = __ffma2_rn(a3, S16S16, MM);    // (e3, e7)
+    __half2 h[4];
+    h[0] = __floats2half2_rn(r0.x, r1.x);   // (e0, e1)
+    h[1] = __floats2half2_rn(r2.x, r3.x);   // (e2, e3)
+    h[2] = __floats2half2_rn(r0.y, r1.y);   // (e4, e5)
+    h[3] = __floats2half2_rn(r2.y, r3.y);   // (e6, e7)
+    return *reinterpret_cast<uint4*>(h);
+}
+
 // ---- IEEE total order helpers (finite values): -0 below +0.
 __device__ __forceinline__ bool total_less(float a, float b) {
     return a < b || (a == b && (__float_as_uint(a) >> 31) > (__float_as_uint(b) >> 31));

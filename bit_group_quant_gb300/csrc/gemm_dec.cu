@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t r[32];
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) {
-                    const uint4 v = dequant8(wd[cc], S, S16, mn);
+                    const uint4 v = dequant8_x2(wd[cc], S, S16, mn);
                     r[4 * cc] = v.x;
                     r[4 * cc + 1] = v.y;
                     r[4 * cc + 2] = v.z;
