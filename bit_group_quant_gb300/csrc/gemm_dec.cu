@@ -279,48 +279,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     // overlap; the parts are added in k order.
     auto y_epilogue = [&](uint32_t acc, int n, int row, int nparts, int c_first, int c_step) {
         const float bias = (p.bias != nullptr && n < p.N) ? __half2float(p.bias[n]) : 0.0f;
-        for (int c0 = 8 * c_first; c0 < p.nt; c0 += 8 * c_step) {
-            uint32_t r[8];
+        const bool nv = n < p.N;
+        // Two 8-column chunks per round (c0 and c0 + 8 c_step): the residual
+        // and partial-sum loads of both are issued before the first add, so
+        // a round costs one L2 round trip for 16 columns.
+        for (int c0 = 8 * c_first; c0 < p.nt; c0 += 16 * c_step) {
+            const int c1 = c0 + 8 * c_step;
+            const bool two = c1 < p.nt;            // warp-uniform
+            uint32_t r0[8], r1[8];
             __syncwarp();   // the stores of the previous round diverge
-            tmem_ld8(acc + static_cast<uint32_t>(c0), r);
+            tmem_ld8(acc + static_cast<uint32_t>(c0), r0);
+            if (two) tmem_ld8(acc + static_cast<uint32_t>(c1), r1);
             tmem_wait_ld();
-            if (n >= p.N) continue;
-            float res[8], v[8];
+            if (!nv) continue;
+            float v0[8], v1[8], res0[8], res1[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                res[j] = (p.residual != nullptr && c0 + j < p.M)
-                             ? __half2float(__ldg(p.residual + static_cast<int64_t>(c0 + j) * p.N + n))
-                             : 0.0f;
-                v[j] = __uint_as_float(r[j]);
+                const bool has_r = p.residual != nullptr;
+                res0[j] = (has_r && c0 + j < p.M)
+                              ? __half2float(__ldg(p.residual + static_cast<int64_t>(c0 + j) * p.N + n))
+                              : 0.0f;
+                res1[j] = (has_r && two && c1 + j < p.M)
+                              ? __half2float(__ldg(p.residual + static_cast<int64_t>(c1 + j) * p.N + n))
+                              : 0.0f;
+                v0[j] = __uint_as_float(r0[j]);
+                v1[j] = two ? __uint_as_float(r1[j]) : 0.0f;
             }
-            for (int p0 = 0; p0 < nparts; p0 += 4) {
-                float pv[4][8];
+            // the later parts, in k order (the first one's loads go out with
+            // the residual's)
+            for (int u = 0; u < nparts; ++u) {
+                const float* src =
+                    p.partial +
+                    static_cast<size_t>((q + 1 + u) * c + static_cast<int>(crank)) * p.nt * kTileF + row;
+                float pv0[8], pv1[8];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const bool has = p0 + u < nparts;
-                    const float* src =
-                        p.partial +
-                        static_cast<size_t>(has ? (q + 1 + p0 + u) * c + static_cast<int>(crank) : 0) *
-                            p.nt * kTileF +
-                        row + c0 * kTileF;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) pv[u][j] = has ? __ldcg(src + j * kTileF) : 0.0f;
+                for (int j = 0; j < 8; ++j) {
+                    pv0[j] = __ldcg(src + (c0 + j) * kTileF);
+                    pv1[j] = two ? __ldcg(src + (c1 + j) * kTileF) : 0.0f;
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (p0 + u < nparts) {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) v[j] = __fadd_rn(v[j], pv[u][j]);
-                    }
+                for (int j = 0; j < 8; ++j) {
+                    v0[j] = __fadd_rn(v0[j], pv0[j]);
+                    v1[j] = __fadd_rn(v1[j], pv1[j]);
+                }
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int m = c0 + j;
-                if (m >= p.M) break;
-                float x = __fadd_rn(v[j], bias);
-                if (p.act == FG_ACT_RELU) x = fmaxf(x, 0.0f);
-                if (p.residual) x = __fadd_rn(x, res[j]);
-                p.Y[static_cast<int64_t>(m) * p.N + n] = __float2half_rn(x);
+            for (int h2 = 0; h2 < 2; ++h2) {
+                if (h2 == 1 && !two) break;
+                const int cb = h2 ? c1 : c0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int m = cb + j;
+                    if (m >= p.M) break;
+                    float x = __fadd_rn(h2 ? v1[j] : v0[j], bias);
+                    if (p.act == FG_ACT_RELU) x = fmaxf(x, 0.0f);
+                    if (p.residual) x = __fadd_rn(x, h2 ? res1[j] : res0[j]);
+                    p.Y[static_cast<int64_t>(m) * p.N + n] = __float2half_rn(x);
+                }
             }
         }
     };
