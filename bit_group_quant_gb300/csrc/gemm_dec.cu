@@ -71,6 +71,7 @@ constexpr int kABase = 2 * kAccStride;  // first TMEM column of the A ring
 constexpr int kNS = 3;                  // stages: A in TMEM, B in shared memory
 constexpr int kG = 3;                   // dequant groups in flight
 constexpr int kSC = 4;                  // codes boxes in flight
+constexpr int kDecMinUnits = 3;         // units (256-k boxes of a tile pair) per cluster, at least
 constexpr int kThreads = 32 * (8 + 4 * kG);
 constexpr uint32_t kCBytes = kTileF * kBoxK / 2;      // 16 KB of packed codes
 constexpr uint32_t kMBytes = kTileF * (kBoxK / 64) * 8;   // 4 KB of (min, scale)
@@ -699,7 +700,14 @@ bool plan_gemm_dec(int64_t M, int64_t N, int64_t K, int64_t plan_rows, GemmPlan&
     pl.dec_c = c;
     pl.dec_nbox = static_cast<int>(K / kBoxK);
     pl.dec_units = static_cast<long long>(F / c) * pl.dec_nbox;
-    pl.dec_Q = static_cast<int>(pl.dec_units < qmax ? pl.dec_units : qmax);
+    // at least kDecMinUnits units per cluster: a small projection (few units)
+    // runs on fewer clusters, so its tiles are split fewer ways and the
+    // tile-finishing epilogues add fewer parts (measured on the small
+    // workloads; the large projections have tens of units per cluster)
+    long long nq = pl.dec_units / kDecMinUnits;
+    if (nq < 1) nq = 1;
+    if (nq > qmax) nq = qmax;
+    pl.dec_Q = static_cast<int>(nq);
     const size_t slots = static_cast<size_t>(pl.dec_Q) * c;
     pl.dec_part_bytes = (slots * pl.nt * kTileF * sizeof(float) + 255) & ~static_cast<size_t>(255);
     pl.ws_bytes = pl.dec_part_bytes + slots * 4 * sizeof(unsigned long long);
