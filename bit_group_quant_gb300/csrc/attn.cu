@@ -998,7 +998,12 @@ __global__ void __launch_bounds__(kDecThreads, kMinBlocks) decode_attn_staged_ke
         const int ntile = ok ? (n + 15) >> 4 : 0;
         for (int kt = warp; kt < ntile; kt += NWARP) {
             const int j0 = kt * 16;
-            int keys[4] = {j0 + 2 * t, j0 + 2 * t + 1, j0 + 2 * t + 8, j0 + 2 * t + 9};
+            // The 16 keys of the tile in any order the P fragment shares: lane t
+            // takes keys j0 + t + 4u.  Rows of 64 code bytes put keys two apart
+            // in the same bank; keys one apart differ by 16 banks, so the four
+            // lanes of a fragment row read at most 2-way conflicting banks (the
+            // pairs 2t, 2t + 1, 2t + 8, 2t + 9 were 4-way).
+            int keys[4] = {j0 + t, j0 + 4 + t, j0 + 8 + t, j0 + 12 + t};
             uint32_t bw[2];
             {
                 float pp[4];
