@@ -39,13 +39,19 @@
 //    release/acquire flag tagged with the launch's epoch), then runs the
 //    epilogue.  The split depends on (N, K) and the number of clusters only,
 //    never on M, so every row's result is independent of the other rows.
+//  * The residual (out and fc2 projections) reaches the epilogue as a tile
+//    in shared memory, loaded by TMA while the segment's main loop runs:
+//    read by each thread from global memory, 2 bytes at a time and late in
+//    the segment, it cost 7-10 % of those launches (measured by leaving the
+//    loads out).
 //
 // Warp roles (640 threads): warp 0 = TMA producer of codes boxes and their
 // (min, scale); warp 1 = TMEM allocator and the single MMA-issuing thread;
 // warp 2 = TMA producer of this CTA's slice of the activation stages
-// (multicast to the cluster); warp 3 idle; warps 4-7 = epilogue, one per TMEM
-// lane quarter; warps 8-19 = dequantisers, group g = warps 8+4g .. 11+4g, the
-// warp of lane quarter q owning weight rows 32q..32q+31 (one row per thread).
+// (multicast to the cluster); warp 3 = TMA producer of residual tiles;
+// warps 4-7 = epilogue, one per TMEM lane quarter; warps 8-19 =
+// dequantisers, group g = warps 8+4g .. 11+4g, the warp of lane quarter q
+// owning weight rows 32q..32q+31 (one row per thread).
 //
 // Every wait (mbarrier or flag) is bounded; a wait that expires flags the CTA
 // to stop, records a timeout in the device status word, waits for its own
@@ -75,6 +81,7 @@ constexpr int kDecMinUnits = 3;         // units (256-k boxes of a tile pair) pe
 constexpr int kThreads = 32 * (8 + 4 * kG);
 constexpr uint32_t kCBytes = kTileF * kBoxK / 2;      // 16 KB of packed codes
 constexpr uint32_t kMBytes = kTileF * (kBoxK / 64) * 8;   // 4 KB of (min, scale)
+constexpr uint32_t kRBytes = kMaxNt * kTileF * 2;         // the residual tile of a Y segment
 static_assert(kABase + kNS * kACols <= 512, "TMEM columns");
 static_assert(kMaxNt <= kAccStride, "accumulator width");
 // A parity wait on an mbarrier tells the current phase from the previous one
@@ -130,9 +137,10 @@ struct SegIter {
 //                                          128-byte swizzled, K-major)
 //   codes   [kSC][128 rows][128 B]       (128-byte swizzled)
 //   meta    [kSC][128 rows][4][2] fp32
+//   resid   [nt][128] fp16                 (residual rows of the current Y tile)
 //   barriers, TMEM address slot, abort flag
 struct Smem {
-    uint32_t base, b0, c0, m0, bars;
+    uint32_t base, b0, c0, m0, r0, bars;
     uint32_t half_bytes;   // nt * 128
     __device__ uint32_t b(int s) const { return b0 + static_cast<uint32_t>(s) * 2u * half_bytes; }
     __device__ uint32_t c(int s) const { return c0 + static_cast<uint32_t>(s) * kCBytes; }
@@ -144,18 +152,24 @@ struct Smem {
     __device__ uint32_t acc_full(int a) const { return bars + 8u * (2 * kNS + 2 * kSC + a); }
     __device__ uint32_t acc_empty(int a) const { return bars + 8u * (2 * kNS + 2 * kSC + 2 + a); }
     __device__ uint32_t drain() const { return bars + 8u * (2 * kNS + 2 * kSC + 4); }
-    __device__ uint32_t end() const { return drain() + 8u; }
+    __device__ uint32_t res_full() const { return bars + 8u * (2 * kNS + 2 * kSC + 5); }
+    __device__ uint32_t res_empty() const { return bars + 8u * (2 * kNS + 2 * kSC + 6); }
+    __device__ uint32_t res_last() const { return bars + 8u * (2 * kNS + 2 * kSC + 7); }
+    __device__ uint32_t end() const { return bars + 8u * (2 * kNS + 2 * kSC + 8); }
 };
 
-__host__ __device__ constexpr size_t dec_smem_bytes(int nt) {
-    return 1024 + static_cast<size_t>(kNS) * 2 * nt * 128 + kSC * (kCBytes + kMBytes) +
-           8 * (2 * kNS + 2 * kSC + 5) + 16;
+// res: the launch has a residual (its tiles are staged in shared memory);
+// without one the L1 cache keeps those 36 KB.
+__host__ __device__ constexpr size_t dec_smem_bytes(int nt, bool res) {
+    return 1024 + static_cast<size_t>(kNS) * 2 * nt * 128 + kSC * (kCBytes + kMBytes) + (res ? kRBytes : 0) +
+           8 * (2 * kNS + 2 * kSC + 8) + 16;
 }
-static_assert(dec_smem_bytes(kMaxNt) <= 227 * 1024, "shared memory");
+static_assert(dec_smem_bytes(kMaxNt, true) <= 227 * 1024, "shared memory");
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_dec_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
-                    const __grid_constant__ CUtensorMap tmM, const DecParams p) {
+                    const __grid_constant__ CUtensorMap tmM, const __grid_constant__ CUtensorMap tmR,
+                    const DecParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     Smem sm;
@@ -164,7 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.b0 = sm.base;
     sm.c0 = sm.b0 + kNS * 2u * sm.half_bytes;
     sm.m0 = sm.c0 + kSC * kCBytes;
-    sm.bars = sm.m0 + kSC * kMBytes;
+    sm.r0 = sm.m0 + kSC * kMBytes;
+    sm.bars = sm.r0 + (p.residual != nullptr ? kRBytes : 0u);
     uint8_t* const gen = smem_raw - raw;   // generic pointer = gen + shared address
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gen + sm.end());
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -204,6 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sm.acc_empty(a), 4);     // the 4 epilogue warps
         }
         mbar_init(sm.drain(), 1);
+        mbar_init(sm.res_full(), 1);
+        mbar_init(sm.res_empty(), 4);   // the 4 epilogue warps, after each Y segment
+        mbar_init(sm.res_last(), 1);
         // A wait that expired earlier (status not yet cleared by fg_check)
         // makes every later cluster skip its work instead of waiting again.
         *abort_flag = (p.status != nullptr && *reinterpret_cast<volatile int*>(p.status) != 0);
@@ -211,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmC);
         prefetch_tmap(&tmM);
+        if (p.residual != nullptr) prefetch_tmap(&tmR);
     }
     __syncthreads();
     // Every barrier of every CTA in the cluster exists before any multicast.
@@ -275,15 +294,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // Y = act(acc + later parts + bias) + residual for one weight row n per
     // thread (the TMEM lanes of its quarter), 8-column chunks c_first,
-    // c_first + c_step, ...  Every load of a chunk is issued before the first
-    // add (residual and partial sums never alias Y), so their latencies
-    // overlap; the parts are added in k order.
+    // c_first + c_step, ...  The residual comes from the segment's tile in
+    // shared memory; every partial-sum load of a round is issued before the
+    // first add, so their latencies overlap; the parts are added in k order.
+    const __half* rbuf = reinterpret_cast<const __half*>(gen + sm.r0);
     auto y_epilogue = [&](uint32_t acc, int n, int row, int nparts, int c_first, int c_step) {
         const float bias = (p.bias != nullptr && n < p.N) ? __half2float(p.bias[n]) : 0.0f;
         const bool nv = n < p.N;
-        // Two 8-column chunks per round (c0 and c0 + 8 c_step): the residual
-        // and partial-sum loads of both are issued before the first add, so
-        // a round costs one L2 round trip for 16 columns.
+        if (nparts >= 2) {
+            // Several later parts: one 8-column chunk per round with up to
+            // three parts' loads in flight together (one L2 round trip for
+            // three parts instead of three).
+            for (int c0 = 8 * c_first; c0 < p.nt; c0 += 8 * c_step) {
+                uint32_t r0[8];
+                __syncwarp();
+                tmem_ld8(acc + static_cast<uint32_t>(c0), r0);
+                tmem_wait_ld();
+                if (!nv) continue;
+                float v0[8], res0[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    res0[j] = (p.residual != nullptr && c0 + j < p.M)
+                                  ? __half2float(rbuf[(c0 + j) * kTileF + row])
+                                  : 0.0f;
+                    v0[j] = __uint_as_float(r0[j]);
+                }
+                for (int u0 = 0; u0 < nparts; u0 += 3) {
+                    float pv[3][8];
+#pragma unroll
+                    for (int u = 0; u < 3; ++u) {
+                        const bool has = u0 + u < nparts;
+                        const float* src =
+                            p.partial +
+                            static_cast<size_t>(has ? (q + 1 + u0 + u) * c + static_cast<int>(crank) : 0) *
+                                p.nt * kTileF +
+                            row + c0 * kTileF;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) pv[u][j] = has ? __ldcg(src + j * kTileF) : 0.0f;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 3; ++u)
+                        if (u0 + u < nparts) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) v0[j] = __fadd_rn(v0[j], pv[u][j]);
+                        }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int m = c0 + j;
+                    if (m >= p.M) break;
+                    float x = __fadd_rn(v0[j], bias);
+                    if (p.act == FG_ACT_RELU) x = fmaxf(x, 0.0f);
+                    if (p.residual) x = __fadd_rn(x, res0[j]);
+                    p.Y[static_cast<int64_t>(m) * p.N + n] = __float2half_rn(x);
+                }
+            }
+            return;
+        }
+        // At most one later part: two 8-column chunks per round (c0 and
+        // c0 + 8 c_step), the part's loads of both issued before the first
+        // add, so a round costs one L2 round trip for 16 columns.
         for (int c0 = 8 * c_first; c0 < p.nt; c0 += 16 * c_step) {
             const int c1 = c0 + 8 * c_step;
             const bool two = c1 < p.nt;            // warp-uniform
@@ -298,10 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 8; ++j) {
                 const bool has_r = p.residual != nullptr;
                 res0[j] = (has_r && c0 + j < p.M)
-                              ? __half2float(__ldg(p.residual + static_cast<int64_t>(c0 + j) * p.N + n))
+                              ? __half2float(rbuf[(c0 + j) * kTileF + row])
                               : 0.0f;
                 res1[j] = (has_r && two && c1 + j < p.M)
-                              ? __half2float(__ldg(p.residual + static_cast<int64_t>(c1 + j) * p.N + n))
+                              ? __half2float(rbuf[(c1 + j) * kTileF + row])
                               : 0.0f;
                 v0[j] = __uint_as_float(r0[j]);
                 v1[j] = two ? __uint_as_float(r1[j]) : 0.0f;
@@ -406,6 +476,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < kNS; ++j)
                 if (issued_last[j] >= 0)
                     mbar_wait(sm.full(j), (issued_last[j] / kNS) & 1, nullptr, lim);
+        }
+    } else if (warp == 3) {
+        if (lane == 0 && p.residual != nullptr) {
+            // ---------------- residual TMA producer: the residual rows of each
+            // segment that ends in the Y epilogue (a whole tile or a tile's
+            // first part), one [nt][128] tile at a time, loaded as soon as
+            // the previous one has been read
+            griddep_wait();
+            SegIter it = proto;
+            int ny = 0, issued = -1;
+            bool last_y = false;
+            while (it.next()) {
+                last_y = false;
+                if (it.b0 != 0) continue;
+                if (!mbar_wait(sm.res_empty(), (ny & 1) ^ 1u, abort_flag, lim)) {
+                    fail();
+                    break;
+                }
+                mbar_arrive_expect_tx(sm.res_full(), static_cast<uint32_t>(p.nt) * kTileF * 2u);
+                tma_load_2d(sm.r0, &tmR, (it.t * c + static_cast<int>(crank)) * kTileF, 0, sm.res_full());
+                issued = ny++;
+                last_y = it.u >= it.hi;
+            }
+            // no copy may land after this CTA leaves; the dequant warps that
+            // share the last Y epilogue wait for its rows here
+            if (issued >= 0 && mbar_wait(sm.res_full(), issued & 1, nullptr, lim) && last_y)
+                mbar_arrive(sm.res_last());
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer.  The whole warp runs the loop (its
@@ -551,6 +648,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     bool ok = true;
                     const int nparts = wait_parts(lt, lb1, qq, ok);
+                    if (ok && p.residual != nullptr)
+                        ok = __all_sync(0xffffffffu, mbar_wait(sm.res_last(), 0, abort_flag, lim));
                     if (ok)
                         y_epilogue(tmem + tl + static_cast<uint32_t>(a * kAccStride),
                                    (lt * c + static_cast<int>(crank)) * kTileF + row, row, nparts,
@@ -570,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tl = static_cast<uint32_t>(qq * 32) << 16;
         const int slot = q * c + static_cast<int>(crank);
         SegIter it = proto;
-        int sg = 0;
+        int sg = 0, ny = 0;
         while (it.next()) {
             const bool last = it.u >= it.hi;
             const int a = sg & 1;
@@ -603,8 +702,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // The tile's first part (or the whole tile); in the last
                 // segment shared with the dequantisers (chunks 0, 4, 8, ...).
                 const int nparts = wait_parts(it.t, it.b1, qq, ok);
+                if (ok && p.residual != nullptr)
+                    ok = __all_sync(0xffffffffu, mbar_wait(sm.res_full(), ny & 1, abort_flag, lim));
                 if (ok) {
                     y_epilogue(acc, n, row, nparts, 0, last ? 4 : 1);
+                    if (p.residual != nullptr) {
+                        // the next tile's TMA (async proxy) overwrites what
+                        // these generic reads saw
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(sm.res_empty());
+                    }
+                    ++ny;
                     if (last) last_nparts = nparts;
                 } else {
                     fail();
@@ -656,7 +765,7 @@ int dec_max_clusters(int c) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     std::lock_guard<std::mutex> lk(mu);
     if (cache[dev][c] == 0) {
-        const size_t smem = dec_smem_bytes(kMaxNt);
+        const size_t smem = dec_smem_bytes(kMaxNt, true);
         if (cudaFuncSetAttribute(gemm_dec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem)) != cudaSuccess)
             return 0;
@@ -723,7 +832,7 @@ fg_status launch_gemm_dec(const __half* X, int64_t M, const fg_q4* W, const __ha
         return set_error(FG_ERR_WORKSPACE, "dequant_gemm: workspace %zu < %zu bytes or misaligned",
                          ws_bytes, pl.ws_bytes);
     const int c = pl.dec_c;
-    CUtensorMap tmX, tmC, tmM;
+    CUtensorMap tmX, tmC, tmM, tmR;
     // activations: this CTA's nt / c rows of a 64-k half stage (rows >= M read as 0)
     fg_status s = make_tmap(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, K, M, 64, pl.nt / c,
                             CU_TENSOR_MAP_SWIZZLE_128B);
@@ -736,6 +845,14 @@ fg_status launch_gemm_dec(const __half* X, int64_t M, const fg_q4* W, const __ha
     s = make_tmap(&tmM, W->meta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (K / 64) * 2, N,
                   (kBoxK / 64) * 2, kTileF, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (s != FG_OK) return s;
+    // residual: the [nt][128] tile of a Y segment (rows >= M, columns >= N read as 0)
+    if (residual != nullptr) {
+        s = make_tmap(&tmR, residual, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, N, M, kTileF, pl.nt,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (s != FG_OK) return s;
+    } else {
+        tmR = tmX;   // never read
+    }
     DecParams p{};
     p.bias = bias;
     p.residual = residual;
@@ -755,9 +872,11 @@ fg_status launch_gemm_dec(const __half* X, int64_t M, const fg_q4* W, const __ha
     p.status = device_status_ptr();
     p.wait_ns = wait_limit_ns();
     p.drop_arrive = take_drop_arrive();
-    const size_t smem = dec_smem_bytes(kMaxNt);   // one CTA per SM whatever nt
+    // one CTA per SM whatever nt; the attribute allows the largest launch (a
+    // graph may hold both kinds), each launch asks for what it uses
+    const size_t smem = dec_smem_bytes(kMaxNt, residual != nullptr);
     cudaError_t e = cudaFuncSetAttribute(gemm_dec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+                                         static_cast<int>(dec_smem_bytes(kMaxNt, true)));
     if (e != cudaSuccess) return cuda_error(e, "gemm_dec smem attribute");
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(pl.dec_Q * c), 1, 1);
@@ -775,7 +894,7 @@ fg_status launch_gemm_dec(const __half* X, int64_t M, const fg_q4* W, const __ha
     // (+ residual); the partial sums of split tiles stay in L2
     TraceScope ts(FG_TRACE_GEMM_DECODE, st, 2.0 * Md * Nd * Kd,
                   Nd * Kd * 0.625 + Md * Kd * 2.0 + Md * Nd * 2.0 * (residual ? 2.0 : 1.0));
-    e = cudaLaunchKernelEx(&cfg, gemm_dec_kernel, tmX, tmC, tmM, p);
+    e = cudaLaunchKernelEx(&cfg, gemm_dec_kernel, tmX, tmC, tmM, tmR, p);
     if (e != cudaSuccess) return cuda_error(e, "gemm_dec launch");
     return cuda_error(cudaGetLastError(), "gemm_dec launch");
 }
