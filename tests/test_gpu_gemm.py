@@ -26,6 +26,10 @@ def _case(M, N, K, seed, wstd=0.02):
     (1, 128, 64), (4, 2304, 768), (16, 768, 3072), (144, 512, 1024),
     (200, 384, 512), (300, 256, 640), (513, 128, 256), (4, 128, 8192),
     (512, 512, 1024), (768, 384, 512),   # 256-row tiles: 3-stage ring, 4- and 1-CTA clusters
+    # decode regime, odd tile counts (1-CTA clusters): a partial last weight
+    # tile and activation rows past M, read as zeros in the staged residual
+    # tile; tiles split over two and three clusters (several later parts)
+    (37, 1040, 512), (130, 2176, 1536),
 ])
 @pytest.mark.parametrize("act,use_bias,use_res", [(0, True, True), (1, True, False), (0, False, False)])
 def test_dequant_gemm_matches_oracle(M, N, K, act, use_bias, use_res):
