@@ -52,3 +52,31 @@ def test_decode_graph_replay_equals_eager(order, padded):
             assert torch.equal(logits[t % 2], kept[t - 1]), t
         fg.fg_check()
         assert torch.equal(toks_g, toks_e)
+
+
+def test_split_tile_gemm_with_residual_graph_replay_bitwise():
+    """A decode-regime projection whose weight tiles are split over clusters
+    (the later parts meet behind flags tagged with the launch's epoch) and
+    whose residual is staged by TMA, recorded in a CUDA graph: every replay
+    (same tag) equals the eager result bit for bit, because the consumed
+    flags are reset after use and each replay waits for its own parts."""
+    M, N, K = 37, 1040, 512   # 9 weight tiles (1-CTA clusters), 18 units over 6 clusters
+    g = synth.generator(600, DEV)
+    x = synth.normal_f16((M, K), 1.0, g, DEV)
+    w = synth.normal_f16((N, K), 0.02, g, DEV)
+    b = synth.normal_f16((N,), 0.1, g, DEV)
+    r = synth.normal_f16((M, N), 1.0, g, DEV)
+    q = fg.fg_quantize_g4(w)
+    ws = torch.empty(max(fg.fg_dequant_gemm_workspace_bytes(M, N, K), 256), dtype=torch.uint8, device=DEV)
+    eager = fg.fg_dequant_gemm_g4(x, q, bias=b, residual=r, workspace=ws)
+    fg.fg_check()
+    y = torch.empty_like(eager)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fg.fg_dequant_gemm_g4(x, q, bias=b, residual=r, Y=y, workspace=ws)
+    for _ in range(3):
+        y.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, eager)
+    fg.fg_check()
