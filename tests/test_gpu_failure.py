@@ -31,27 +31,30 @@ def short_waits():
         pass
 
 
-# M 16 with K a multiple of 256: the TMEM-operand kernel; M 200: one token
-# tile with K split across CTAs; M 300: whole tiles; M 8192: the weights
-# dequantised once, then the CTA-pair GEMM
-@pytest.mark.parametrize("M,N,K", [(16, 512, 1024), (200, 384, 512), (300, 256, 640),
-                                   (8192, 384, 512)])
-def test_dropped_arrive_reports_timeout_and_context_survives(short_waits, M, N, K):
+# M 16 with K a multiple of 256: the TMEM-operand kernel (also with a
+# residual, whose tiles a TMA warp stages: its waits must end too); M 200:
+# one token tile with K split across CTAs; M 300: whole tiles; M 8192: the
+# weights dequantised once, then the CTA-pair GEMM
+@pytest.mark.parametrize("M,N,K,res", [(16, 512, 1024, False), (16, 512, 1024, True),
+                                       (200, 384, 512, False), (300, 256, 640, False),
+                                       (8192, 384, 512, False)])
+def test_dropped_arrive_reports_timeout_and_context_survives(short_waits, M, N, K, res):
     g = synth.generator(M + N + K, DEV)
     x = synth.normal_f16((M, K), 1.0, g, DEV)
     q = fg.fg_quantize_g4(synth.normal_f16((N, K), 0.02, g, DEV))
-    good = fg.fg_dequant_gemm_g4(x, q)
+    r = synth.normal_f16((M, N), 1.0, g, DEV) if res else None
+    good = fg.fg_dequant_gemm_g4(x, q, residual=r)
     fg.fg_check()
     ref = to_np(good).copy()
 
     fg.fg_debug_set(fg.FG_KNOB_DROP_ARRIVE, 1)
     bad = torch.zeros_like(good)
-    fg.fg_dequant_gemm_g4(x, q, Y=bad)           # box 0 never armed: waits expire
-    fg.fg_dequant_gemm_g4(x, q, Y=torch.empty_like(good))   # status set: skips its work
+    fg.fg_dequant_gemm_g4(x, q, residual=r, Y=bad)   # box 0 never armed: waits expire
+    fg.fg_dequant_gemm_g4(x, q, residual=r, Y=torch.empty_like(good))   # status set: skips its work
     with pytest.raises(fg.FgError) as e:
         fg.fg_check()
     assert e.value.status == fg.FG_ERR_TIMEOUT
 
-    again = fg.fg_dequant_gemm_g4(x, q)          # knob consumed, status cleared
+    again = fg.fg_dequant_gemm_g4(x, q, residual=r)   # knob consumed, status cleared
     fg.fg_check()
     assert np.array_equal(to_np(again), ref)
