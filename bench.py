@@ -440,6 +440,7 @@ def run_fg(args, ws, rank, local):
                      "avg_launch_ms": gp["ms"] / max(gp["launches"], 1)},
         "decode_roofline": {
             "gemm": {"bound": "tensor", "achieved": tflops(gd), "unit": "TFLOP/s",
+                     "peak": peak,
                      "frac": tflops(gd) / peak if tflops(gd) else None},
             "attn": {"bound": "hbm", "achieved": gbs(ad), "unit": "GB/s",
                      "peak": peaks["hbm_gbs"],
