@@ -177,9 +177,11 @@ fg_status fg_dequant_g4(const fg_q4* in, fg_f16* x, fg_stream stream);
  * of the decoder ("FlexGen 完全拆解", dataflow section: K = XW_K etc.).
  * X: [M][K] fp16 (K = W->cols), row stride K, 16-byte aligned.
  * W: [N][K] 4-bit (N = W->rows).  bias: [N] fp16 or NULL.
- * residual: [M][N] fp16 or NULL (may alias neither X nor Y).
+ * residual: [M][N] fp16 or NULL (may alias neither X nor Y), 16-byte
+ * aligned (tiles of it are copied by TMA).
  * act: FG_ACT_NONE or FG_ACT_RELU (applied to acc + bias, before residual).
- * Y: [M][N] fp16.  M >= 0 (M == 0 launches nothing); N % 16 == 0.
+ * Y: [M][N] fp16, 16-byte aligned.  M >= 0 (M == 0 launches nothing);
+ * N % 16 == 0.  FG_ERR_ALIGN for a misaligned X, Y or residual.
  * workspace: device scratch of at least
  * fg_dequant_gemm_workspace_bytes(M, N, K) bytes (NULL allowed when that is
  * 0), 256-byte aligned.  From M = 8192 rows that size is 2*N*K bytes: the
