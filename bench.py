@@ -228,6 +228,42 @@ MULTI_GPU_REFUSAL = ("one GPU per run: the dequant-GEMM kernels use cluster-mult
                      "single-GPU jobs instead")
 
 
+def workload_config(wl, args, ws, wbytes=None, kvbytes=None):
+    """The `config` object of a bench line: the workload and the options, with
+    the weight and cache footprints computed from the shapes when not given
+    (the oracle's line names the same configuration as the GPU arm's)."""
+    D = wl.decode_steps
+    if wl.vocab == 0:   # one decoder layer fed synthetic hidden states
+        return {"workload": "%s: one decoder layer, h1 %d, %d heads, h2 %d; gbs %d x k %d, "
+                            "s %d, %d teacher-forced decode steps; weights and KV 4-bit g64"
+                            % (wl.name, wl.h1, wl.H, wl.h2, wl.gbs, wl.k, wl.s, D),
+                "decode_launch": "eager" if args.no_graphs else "one CUDA graph per decode step",
+                "l2": "inputs smaller than L2 (a latency-bound workload; no flush)"}
+    host = args.weights == "host"
+    graphs = not args.no_graphs and not host
+    if wbytes is None:   # codes (half a byte) + (min, scale) (8 bytes per 64) per weight
+        wbytes = wl.layers * (4 * wl.h1 * wl.h1 + 2 * wl.h1 * wl.h2) * 0.625
+    if kvbytes is None:  # K and V of every layer, cap = s + n slots
+        per = 2 * wl.d * 2 if args.kv == "f16" else wl.d * 1.25
+        kvbytes = wl.layers * wl.bls * wl.H * wl.cap * per
+    return {"workload": "%s-shaped: %d layers, h1 %d, %d heads, h2 %d, vocab %d; "
+                        "gbs %d x k %d = bls %d, s %d, n %d (%d decode steps); "
+                        "weights 4-bit g64, KV cache %s, in HBM"
+                        % (wl.name, wl.layers, wl.h1, wl.H, wl.h2, wl.vocab, wl.gbs,
+                           wl.k, wl.bls, wl.s, wl.n, D,
+                           "fp16 (uncompressed)" if args.kv == "f16" else "4-bit g64"),
+            "kv_cache": args.kv,
+            "decode_attention": ("top-K sparse, %d%% of the rows' V" % args.topk
+                                 if 0 < args.topk < 100 else "dense"),
+            "order": args.order, "decoding": "greedy (argmax on the device)",
+            "decode_launch": "one CUDA graph per decode step" if graphs else "eager",
+            "parallelism": "replicas" if ws > 1 else "single",
+            "weights": ("4-bit, pinned host memory, streamed one layer ahead over "
+                        "NVLink-C2C" if host else "4-bit, resident in HBM"),
+            "l2": "inputs larger than L2 (weights %.1f GB, KV %.1f GB)"
+                  % (wbytes / 1e9, kvbytes / 1e9)}
+
+
 def run_fg(args, ws, rank, local):
     if ws > 1:
         # no GPU is touched; rank 0 alone says why
@@ -407,22 +443,8 @@ def run_fg(args, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": t_all_max / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
         "data": "synthetic",
-        "config": {"workload": "%s-shaped: %d layers, h1 %d, %d heads, h2 %d, vocab %d; "
-                               "gbs %d x k %d = bls %d, s %d, n %d (%d decode steps); "
-                               "weights 4-bit g64, KV cache %s, in HBM"
-                               % (wl.name, wl.layers, wl.h1, wl.H, wl.h2, wl.vocab, wl.gbs,
-                                  wl.k, wl.bls, wl.s, wl.n, D,
-                                  "fp16 (uncompressed)" if args.kv == "f16" else "4-bit g64"),
-                   "kv_cache": args.kv,
-                   "decode_attention": ("top-K sparse, %d%% of the rows' V" % args.topk
-                                        if 0 < args.topk < 100 else "dense"),
-                   "order": args.order, "decoding": "greedy (argmax on the device)",
-                   "decode_launch": "one CUDA graph per decode step" if graphs else "eager",
-                   "parallelism": "replicas" if ws > 1 else "single",
-                   "weights": ("4-bit, pinned host memory, streamed one layer ahead over "
-                               "NVLink-C2C" if host else "4-bit, resident in HBM"),
-                   "l2": "inputs larger than L2 (weights %.1f GB, KV %.1f GB)"
-                         % (wbytes / 1e9, sum(c.nbytes for c in model.stack.caches) / 1e9)},
+        "config": workload_config(wl, args, ws, wbytes,
+                                  sum(c.nbytes for c in model.stack.caches)),
         "generation_tokens_per_s": gen_value,
         "gemm_tflops": {"prefill": tflops(gp), "decode": tflops(gd)},
         "attn_gbs": {("decode_f16" if args.kv == "f16" else "decode_4bit"): gbs(ad)},
@@ -810,11 +832,7 @@ def run_layer_workload(args, wl, local):
             "warmup": args.warmup, "ms_per_step": (t_pre + t_dec) / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
             "data": "synthetic",
-            "config": {"workload": "%s: one decoder layer, h1 %d, %d heads, h2 %d; gbs %d x k %d, "
-                                   "s %d, %d teacher-forced decode steps; weights and KV 4-bit g64"
-                                   % (wl.name, wl.h1, wl.H, wl.h2, wl.gbs, wl.k, wl.s, D),
-                       "decode_launch": "one CUDA graph per decode step" if graphs else "eager",
-                       "l2": "inputs smaller than L2 (a latency-bound workload; no flush)"},
+            "config": workload_config(wl, args, 1),
             "phase_ms_per_step": {"prefill": t_pre / args.steps * 1e3,
                                   "decode": t_dec / args.steps * 1e3},
             "gpu_launches": int(launches_eager) * args.steps,
@@ -844,7 +862,7 @@ def run_reference(args, ws, rank):
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": "%s-shaped, bls %d, s %d, n %d" % (wl.name, wl.bls, wl.s, wl.n)},
+            "config": workload_config(wl, args, ws),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
