@@ -228,6 +228,16 @@ MULTI_GPU_REFUSAL = ("one GPU per run: the dequant-GEMM kernels use cluster-mult
                      "single-GPU jobs instead")
 
 
+def footprints(wl, kv="g4"):
+    """Bytes of the model's 4-bit weights (codes, half a byte, plus (min,
+    scale), 8 bytes per 64 weights) and of its K/V caches (every layer, cap =
+    s + n slots; 4-bit rows of d/2 code bytes and d/8 (min, scale) bytes, or
+    fp16 rows)."""
+    wbytes = wl.layers * (4 * wl.h1 * wl.h1 + 2 * wl.h1 * wl.h2) * 0.625
+    per = 2 * wl.d * 2 if kv == "f16" else wl.d * 1.25   # K and V together
+    return wbytes, wl.layers * wl.bls * wl.H * wl.cap * per
+
+
 def workload_config(wl, args, ws, wbytes=None, kvbytes=None):
     """The `config` object of a bench line: the workload and the options, with
     the weight and cache footprints computed from the shapes when not given
@@ -241,11 +251,9 @@ def workload_config(wl, args, ws, wbytes=None, kvbytes=None):
                 "l2": "inputs smaller than L2 (a latency-bound workload; no flush)"}
     host = args.weights == "host"
     graphs = not args.no_graphs and not host
-    if wbytes is None:   # codes (half a byte) + (min, scale) (8 bytes per 64) per weight
-        wbytes = wl.layers * (4 * wl.h1 * wl.h1 + 2 * wl.h1 * wl.h2) * 0.625
-    if kvbytes is None:  # K and V of every layer, cap = s + n slots
-        per = 2 * wl.d * 2 if args.kv == "f16" else wl.d * 1.25
-        kvbytes = wl.layers * wl.bls * wl.H * wl.cap * per
+    fw, fkv = footprints(wl, args.kv)
+    wbytes = fw if wbytes is None else wbytes
+    kvbytes = fkv if kvbytes is None else kvbytes
     return {"workload": "%s-shaped: %d layers, h1 %d, %d heads, h2 %d, vocab %d; "
                         "gbs %d x k %d = bls %d, s %d, n %d (%d decode steps); "
                         "weights 4-bit g64, KV cache %s, in HBM"
